@@ -1,0 +1,347 @@
+"""Benchmark of the FP8 fine-grained-scaled GEMM hot path on GB300.
+
+One step = the whole path over one batch: 1x128 quantisation of the fp32
+activations (dg_quant_act_1x128) followed by the FP8 GEMM with two-level
+accumulation and bf16 output (dg_fp8_gemm_nt); the weights are quantised once,
+offline, before timing (dg_quant_weight_128x128).  Default workload: the
+skinny dense GEMM M=256, N=7168, K=2048 with 1% x20 outliers in A.
+
+Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on the
+host cores instead (a bounded row sample of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "FP8 GEMM TFLOPS (2MNK) and fraction of GB300 FP8/HBM roofline, 1 GPU"
+UNIT = "TFLOP/s"
+FP8_PER_BF16 = 2.0           # nominal dense fp8 : bf16 tensor ratio (4.5 : 2.25 PFLOP/s)
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="dg", choices=["dg", "reference"])
+    ap.add_argument("--workload", default="skinny", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks --
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = max(smax, float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- workload ---
+def describe(w: wl.Workload) -> str:
+    if w.layout == "dense":
+        return (f"dense NT FP8 GEMM M={w.M} N={w.N} K={w.K}" + (" (1% x20 outliers in A)" if w.outliers else "")
+                + "; step = 1x128 activation quantisation + GEMM")
+    if w.layout == "contiguous":
+        return f"MoE contiguous FP8 GEMM G={w.G} tokens={w.tokens} N={w.N} K={w.K}; step = quantisation + GEMM"
+    return f"MoE masked FP8 GEMM G={w.G} max_m={w.max_m} N={w.N} K={w.K}; step = quantisation + GEMM"
+
+
+def gemm_shape(w: wl.Workload):
+    """(rows of A, useful rows, N, K, G)."""
+    if w.layout == "dense":
+        return w.M, w.M, w.N, w.K, 1
+    if w.layout == "contiguous":
+        counts, m_indices, _ = wl.contiguous_routing(w.G, w.tokens, w.seed)
+        return len(m_indices), int(counts.sum()), w.N, w.K, w.G
+    mm = wl.masked_counts(w.G, w.max_m, w.seed)
+    return w.G * w.max_m, int(mm.sum()), w.N, w.K, w.G
+
+
+def algorithmic_bytes(w: wl.Workload):
+    """Bytes the GEMM must move at least once: A + B (+ scales) + D, counting
+    only useful rows and experts that have any."""
+    rows_total, useful, N, K, G = gemm_shape(w)
+    KB = K // 128
+    NB = -(-N // 128)
+    if w.layout == "masked":
+        mm = wl.masked_counts(w.G, w.max_m, w.seed)
+        experts = int((mm > 0).sum())
+    else:
+        experts = G
+    return useful * K + experts * N * K + useful * KB * 4 + experts * NB * KB * 4 + useful * N * 2
+
+
+# ---------------------------------------------------------------- CPU leg --
+def cpu_oracle_rate(w: wl.Workload, seconds: float):
+    """Time the oracle (quantise + GEMM) on whole rows of the workload until
+    about `seconds` have passed; returns (TFLOP/s, rows, elapsed, threads)."""
+    import oracle
+    if w.layout != "dense":
+        raise SystemExit("the CPU baseline leg covers the dense workloads")
+    x, wt = wl.dense_inputs(w.M, w.N, w.K, w.seed, w.outliers)
+    qb, sfb = oracle.quant_weight_128x128(wt)
+    rows_done, elapsed, chunk = 0, 0.0, 8
+    while elapsed < seconds and rows_done < w.M:
+        r1 = min(w.M, rows_done + chunk)
+        t0 = time.perf_counter()
+        qa, sfa = oracle.quant_act_1x128(x[rows_done:r1])
+        oracle.gemm_nt(qa, sfa, qb, sfb)
+        elapsed += time.perf_counter() - t0
+        rows_done = r1
+        chunk = min(chunk * 2, 64)
+    flops = 2.0 * rows_done * w.N * w.K
+    return flops / elapsed / 1e12, rows_done, elapsed, oracle.num_threads()
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    rates = []
+    rows = 0
+    per_step = max(1.0, args.cpu_seconds / max(args.steps, 1))
+    for i in range(args.warmup + args.steps):
+        rate, rows, el, thr = cpu_oracle_rate(w, per_step if i >= args.warmup else 0.2)
+        if i >= args.warmup:
+            rates.append(rate)
+    value = statistics.mean(rates)
+    rows_total = gemm_shape(w)[0]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 2.0 * gemm_shape(w)[1] * w.N * w.K / (value * 1e12) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 block sums, fp32 promotion",
+        "data": "synthetic", "config": {"workload": describe(w)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
+                         "sample": f"first {rows} of {rows_total} rows per step (quantise + GEMM), "
+                                   f"rate scaled to the full workload"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU leg --
+def run_gpu(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import moe_grouped_gemm_x128_gb300 as dg
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dg.build()
+    dg.load()
+    if w.layout != "dense":
+        raise SystemExit("bench.py times the dense workloads; grouped layouts are covered by the tests")
+    M, N, K = w.M, w.N, w.K
+    dev = torch.device("cuda", local)
+
+    # inputs: several independent sets so that consecutive steps do not hit L2
+    x_host, w_host = wl.dense_inputs(M, N, K, w.seed, w.outliers)
+    set_bytes = M * K * 4 + M * K + N * K + M * N * 2
+    n_sets = max(2, -(-2 * L2_BYTES // set_bytes))
+    xs, qas, sfas, qbs, sfbs, ds = [], [], [], [], [], []
+    wt = torch.from_numpy(w_host).to(dev)
+    for i in range(n_sets):
+        xs.append(torch.from_numpy(x_host).to(dev))
+        qb, sfb = dg.dg_quant_weight_128x128(wt)
+        qbs.append(qb)
+        sfbs.append(sfb)
+        qas.append(torch.empty((M, K), dtype=torch.uint8, device=dev))
+        sfas.append(torch.zeros((K // 128, dg.round_up(M, 4)), dtype=torch.float32, device=dev))
+        ds.append(torch.empty((M, N), dtype=torch.bfloat16, device=dev))
+    del wt
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        j = i % n_sets
+        dg.dg_quant_act_1x128(xs[j], qas[j], sfas[j])
+        if ev is not None:
+            ev.record(stream)
+        dg.dg_fp8_gemm_nt(qas[j], sfas[j], qbs[j], sfbs[j], ds[j])
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    # timed region: K steps; events split each step into quantiser | GEMM
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps + 1)]
+    with ClockSampler(local) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        for i in range(args.steps):
+            step(i, ev[2 * i + 1])
+            ev[2 * i + 2].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    total_ms = ev[0].elapsed_time(ev[-1])
+    quant_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps))
+    gemm_ms = sum(ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(args.steps))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end to end: pinned host activations in, bf16 result out, every step
+    x_pin = torch.from_numpy(x_host).pin_memory()
+    d_pin = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    for i in range(2):
+        xs[0].copy_(x_pin, non_blocking=True)
+        step(0)
+        d_pin.copy_(ds[0], non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        j = i % n_sets
+        xs[j].copy_(x_pin, non_blocking=True)
+        step(i)
+        d_pin.copy_(ds[j], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+
+    flops_step = 2.0 * M * N * K
+    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    e2e_value = world * flops_step * args.steps / (e2e_ms * 1e-3) / 1e12
+
+    hbm, bf16, bf16_sus, src = peaks()
+    fp8_peak = bf16 * FP8_PER_BF16
+    gemm_s = gemm_ms / args.steps * 1e-3
+    ab = algorithmic_bytes(w)
+    t_mem = ab / (hbm * 1e9)
+    t_cmp = flops_step / (fp8_peak * 1e12)
+    if t_mem >= t_cmp:
+        roof = {"bound": "hbm", "achieved": ab / gemm_s / 1e9, "peak": hbm, "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops_step / gemm_s / 1e12, "peak": fp8_peak, "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["peak_source"] = f"{src} (MEASURED_PEAKS.json; fp8 = bf16 x {FP8_PER_BF16:g})" if src == "measured" \
+        else "fallback"
+    roof["kernel"] = "fp8_gemm_kernel"
+    roof["kernel_us"] = gemm_s * 1e6
+    roof["quant_us"] = quant_ms / args.steps * 1e3
+    roof["algorithmic_bytes"] = ab
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": describe(w), "l2": f"rotating {n_sets} input sets of {set_bytes / 1e6:.1f} MB "
+                                                  f"(> 2x L2) between steps",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": M * K * 4, "d2h_bytes_per_step": M * N * 2},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, rows, el, thr = cpu_oracle_rate(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": thr, "kind": "oracle",
+                                "sample": f"oracle quantise + GEMM on the first {rows} of {M} rows "
+                                          f"({el:.1f} s), rate scaled to TFLOP/s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,649 @@
+// FP8 (E4M3) GEMM with fine-grained scaling and two-level accumulation on the
+// sm_103a tensor cores, for the dense, MoE-contiguous and MoE-masked layouts.
+//
+// What it computes ("DeepGEMM：一款支持FP8通用矩阵乘法(GEMM)的开源库", 技术细节/两级累加技术
+// and 功能特色/细粒度缩放功能): for every 128-wide K block kb the tensor cores form the
+// block's partial product P_kb = A[:, kb] . B[:, kb]^T in fp32 in tensor memory,
+// and the CUDA cores promote it,
+//     acc[m,n] = fmaf(P_kb[m,n], sfa[kb][m] * sfb[n/128][kb], acc[m,n]),
+// kb ascending; D = bf16_rn(acc).
+//
+// How (the page's 线程专业化技术 and 统一的计算任务调度系统, redone for GB300):
+// a persistent kernel, one CTA per SM, 256 threads in four roles:
+//   warp 0      TMA producer: streams A[128x128], B[BNx128] (128-byte swizzled)
+//               and the 128 SFA scales of each K block into an S-stage ring;
+//   warp 1      MMA issuer: one thread issues 4 x tcgen05.mma kind::f8f6f4
+//               (128 x BN x 32) per K block into one of two TMEM partial
+//               buffers (the first with accumulate off, so each K block starts
+//               from zero), then commits to the ring's "empty" barrier and the
+//               buffer's "full" barrier;
+//   warp 2      allocates / frees the TMEM columns;
+//   warps 4-7   epilogue: each thread owns one output row (TMEM lane); per K
+//               block it loads the partial row from TMEM, scales and FMAs it
+//               into fp32 registers, and releases the buffer, so the MMA of
+//               block kb+1 overlaps the promotion of block kb; after the last
+//               block it converts to bf16 and stores the row.
+// Tiles are visited in a grouped order (GROUP_M m-blocks per band) so that the
+// CTAs running at the same time share A and B tiles through L2.
+//
+// Every wait is bounded: after kWaitTimeoutNs a role raises the CTA's abort
+// flag and DG_DEVFLAG_TIMEOUT, the producer waits (bounded) for its own copies
+// in flight, the MMA thread drains its MMAs, TMEM is freed and the CTA exits.
+#include "dg_common.h"
+#include "dg_ptx.cuh"
+
+namespace dg {
+namespace {
+
+constexpr int kBM = 128;                   // rows per tile (tcgen05 M)
+constexpr int kBK = 128;                   // K per stage = one promotion block = one 128-byte row
+constexpr int kMmaK = 32;                  // K per tcgen05.mma for 8-bit inputs
+constexpr int kThreads = 256;
+constexpr int kEpiWarp0 = 4;
+constexpr int kNumEpiWarps = 4;
+constexpr int kGroupM = 16;                // m-blocks per rasterisation band
+constexpr int kMaxMaskedGroups = 1024;     // G limit of the masked layout (tile prefix in smem)
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+
+template <int BN, int STAGES>
+struct SmemLayout {
+    static constexpr int kABytes = kBM * kBK;       // 16 KiB
+    static constexpr int kBBytes = BN * kBK;
+    static constexpr int kSfaBytes = kBM * 4;
+    static constexpr int kAOff = 0;
+    static constexpr int kBOff = kAOff + STAGES * kABytes;
+    static constexpr int kSfaOff = kBOff + STAGES * kBBytes;
+    static constexpr int kBarOff = kSfaOff + STAGES * kSfaBytes;
+    // full[S], empty[S], tfull[2], tempty[2], drain
+    static constexpr int kNumBars = 2 * STAGES + 5;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;   // tmem base, abort flag
+    static constexpr int kPrefixOff = kMiscOff + 16;
+    static constexpr int kBytes = kPrefixOff + (kMaxMaskedGroups + 1) * 4;
+    static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1024
+};
+
+struct Problem {
+    int M;        // dense: rows; contiguous: sum_M; masked: max_m
+    int N;
+    int K;
+    int G;
+    int layout;
+};
+
+struct TileInfo {
+    int g;
+    int m0;        // first row of the tile within its expert's rows
+    int n0;
+    int rows;      // rows of the tile that are inside the problem
+    bool skip;
+};
+
+__device__ __forceinline__ void raise_status(unsigned int *status, unsigned int bit)
+{
+    atomicOr(status, bit);
+}
+
+// Bounded wait for the phase of `bar` with the given parity.  Gives up when
+// another role aborted or after kWaitTimeoutNs.
+__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                        unsigned int *status)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 15u) == 0) {
+            if (*abort_flag)
+                return false;
+            if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+                *abort_flag = 1;
+                raise_status(status, DG_DEVFLAG_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait used while shutting down after an abort (ignores the flag).
+__device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > kWaitTimeoutNs)
+            return;
+}
+
+template <int BN>
+struct Sched {
+    int m_blocks;     // dense / contiguous: m-blocks of the whole problem
+    int n_blocks;
+    int num_tiles;
+    const int *prefix;   // masked: tile prefix per expert (smem)
+    int G;
+
+    __device__ __forceinline__ TileInfo tile(int t, const Problem &p, const int32_t *meta) const
+    {
+        TileInfo ti;
+        ti.skip = false;
+        if (p.layout == DG_LAYOUT_MASKED) {
+            int lo = 0, hi = G;   // find g with prefix[g] <= t < prefix[g+1]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (prefix[mid] <= t)
+                    lo = mid;
+                else
+                    hi = mid;
+            }
+            const int g = lo;
+            const int local = t - prefix[g];
+            const int valid = (prefix[g + 1] - prefix[g]) / n_blocks;   // m-blocks of expert g
+            const int mb = local % valid;
+            const int nb = local / valid;
+            int mm = meta[g];
+            mm = mm < 0 ? 0 : (mm > p.M ? p.M : mm);
+            ti.g = g;
+            ti.m0 = mb * kBM;
+            ti.n0 = nb * BN;
+            ti.rows = min(kBM, mm - ti.m0);
+            return ti;
+        }
+        // grouped rasterisation: bands of kGroupM m-blocks, m fastest inside a band
+        const int band_tiles = kGroupM * n_blocks;
+        const int band = t / band_tiles;
+        const int first_m = band * kGroupM;
+        const int band_m = min(m_blocks - first_m, kGroupM);
+        const int local = t - band * band_tiles;
+        const int mb = first_m + local % band_m;
+        const int nb = local / band_m;
+        ti.m0 = mb * kBM;
+        ti.n0 = nb * BN;
+        ti.rows = min(kBM, p.M - ti.m0);
+        ti.g = 0;
+        if (p.layout == DG_LAYOUT_CONTIGUOUS) {
+            const int g = meta[ti.m0];
+            ti.g = g;
+            ti.skip = (g < 0 || g >= p.G);
+        }
+        return ti;
+    }
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                    const __grid_constant__ CUtensorMap tmap_sfa, const float *__restrict__ sfb,
+                    uint16_t *__restrict__ d, const int32_t *__restrict__ meta, Problem p,
+                    unsigned int *status)
+{
+    using L = SmemLayout<BN, STAGES>;
+    constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+                                   : (2 * BN <= 256)                     ? 256
+                                                                         : 512;
+    constexpr uint32_t kStageTx = L::kABytes + L::kBBytes + L::kSfaBytes;
+    constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, BN);
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 32 in [32, 256]");
+    static_assert(BN % 128 == 0 || 128 % BN == 0, "a 32-column chunk must not straddle two 128-column scale blocks");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + L::kBarOff;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::kMiscOff + 4);
+    int *prefix = reinterpret_cast<int *>(smem + L::kPrefixOff);
+    const float *sfa_smem = reinterpret_cast<const float *>(smem + L::kSfaOff);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int KB = p.K / kBK;
+    const int NBs = (p.N + 127) / 128;   // 128-column scale blocks of B
+
+    // ---------------------------------------------------------------- setup
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1 + kNumEpiWarps);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), kNumEpiWarps);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    Sched<BN> sch;
+    sch.n_blocks = (p.N + BN - 1) / BN;
+    sch.G = p.G;
+    sch.prefix = prefix;
+    if (p.layout == DG_LAYOUT_MASKED) {
+        // per-expert tile counts from masked_m, read on the device
+        if (warp == 3) {
+            const int max_mb = (p.M + kBM - 1) / kBM;
+            int running = 0;
+            for (int base = 0; base < p.G; base += 32) {
+                const int g = base + lane;
+                int cnt = 0;
+                if (g < p.G) {
+                    int mm = meta[g];
+                    if (mm < 0 || mm > p.M) {
+                        raise_status(status, DG_DEVFLAG_MASKED_M_CLAMPED);
+                        mm = mm < 0 ? 0 : p.M;
+                    }
+                    cnt = min((mm + kBM - 1) / kBM, max_mb) * sch.n_blocks;
+                }
+                int incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o)
+                        incl += v;
+                }
+                if (g < p.G)
+                    prefix[g + 1] = running + incl;
+                running += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0)
+                prefix[0] = 0;
+        }
+        sch.m_blocks = 0;
+    } else {
+        sch.m_blocks = (p.M + kBM - 1) / kBM;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    sch.num_tiles = (p.layout == DG_LAYOUT_MASKED) ? prefix[p.G] : sch.m_blocks * sch.n_blocks;
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_a);
+            tma_prefetch_desc(&tmap_b);
+            tma_prefetch_desc(&tmap_sfa);
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t pending = 0;        // stages with a copy whose consumption was not yet observed
+            uint32_t pending_par = 0;    // full-barrier parity of each pending copy
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < sch.num_tiles; t += gridDim.x) {
+                const TileInfo ti = sch.tile(t, p, meta);
+                if (ti.skip)
+                    continue;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    pending &= ~(1u << stage);
+                    const uint32_t fb = full_bar(stage);
+                    mbar_arrive_expect_tx(fb, kStageTx);
+                    const uint32_t a_dst = sbase + L::kAOff + stage * L::kABytes;
+                    const uint32_t b_dst = sbase + L::kBOff + stage * L::kBBytes;
+                    const uint32_t s_dst = sbase + L::kSfaOff + stage * L::kSfaBytes;
+                    const int k0 = kb * kBK;
+                    if (p.layout == DG_LAYOUT_DENSE) {
+                        tma_load_2d(a_dst, &tmap_a, fb, k0, ti.m0);
+                        tma_load_2d(b_dst, &tmap_b, fb, k0, ti.n0);
+                        tma_load_2d(s_dst, &tmap_sfa, fb, ti.m0, kb);
+                    } else if (p.layout == DG_LAYOUT_CONTIGUOUS) {
+                        tma_load_2d(a_dst, &tmap_a, fb, k0, ti.m0);
+                        tma_load_3d(b_dst, &tmap_b, fb, k0, ti.n0, ti.g);
+                        tma_load_2d(s_dst, &tmap_sfa, fb, ti.m0, kb);
+                    } else {
+                        tma_load_3d(a_dst, &tmap_a, fb, k0, ti.m0, ti.g);
+                        tma_load_3d(b_dst, &tmap_b, fb, k0, ti.n0, ti.g);
+                        tma_load_3d(s_dst, &tmap_sfa, fb, ti.m0, kb, ti.g);
+                    }
+                    pending |= 1u << stage;
+                    pending_par = (pending_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // let the copies already issued land before the CTA exits
+                for (int s = 0; s < STAGES; ++s)
+                    if (pending & (1u << s))
+                        drain_wait(full_bar(s), (pending_par >> s) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t tcount = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < sch.num_tiles; t += gridDim.x) {
+                const TileInfo ti = sch.tile(t, p, meta);
+                if (ti.skip)
+                    continue;
+                for (int kb = 0; kb < KB; ++kb) {
+                    const uint32_t buf = tcount & 1u;
+                    const uint32_t tph = (tcount >> 1) & 1u;
+                    if (!wait_phase(tempty_bar(buf), tph ^ 1u, abort_flag, status) ||
+                        !wait_phase(full_bar(stage), phase, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = sbase + L::kAOff + stage * L::kABytes;
+                    const uint32_t b_addr = sbase + L::kBOff + stage * L::kBBytes;
+                    const uint32_t d_tmem = tmem_base + buf * BN;
+#pragma unroll
+                    for (int k = 0; k < kBK / kMmaK; ++k)
+                        mma_f8f6f4(d_tmem, smem_desc_sw128(a_addr + k * kMmaK), smem_desc_sw128(b_addr + k * kMmaK),
+                                   kIdesc, k > 0 ? 1u : 0u);
+                    mma_commit(empty_bar(stage));
+                    mma_commit(tfull_bar(buf));
+                    ++tcount;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // every MMA issued above has completed once this barrier flips
+            mma_commit(drain_bar);
+            drain_wait(drain_bar, 0);
+        }
+    } else if (warp >= kEpiWarp0) {
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;                 // TMEM lane quarter of this warp
+        const int r = q * 32 + lane;            // row of the tile owned by this thread
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t tcount = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < sch.num_tiles; t += gridDim.x) {
+            const TileInfo ti = sch.tile(t, p, meta);
+            if (ti.skip) {
+                if (ti.g >= p.G && threadIdx.x == kEpiWarp0 * 32)
+                    raise_status(status, DG_DEVFLAG_BAD_EXPERT);
+                continue;
+            }
+            // where this thread's row goes, and whether it is written at all
+            bool row_ok = r < ti.rows;
+            size_t d_row = 0;
+            if (p.layout == DG_LAYOUT_MASKED) {
+                d_row = static_cast<size_t>(ti.g) * p.M + ti.m0 + r;
+            } else {
+                d_row = static_cast<size_t>(ti.m0) + r;
+                if (p.layout == DG_LAYOUT_CONTIGUOUS && row_ok) {
+                    const int gr = __ldg(meta + ti.m0 + r);
+                    if (gr != ti.g) {
+                        if (gr >= 0)
+                            raise_status(status, DG_DEVFLAG_MIXED_BLOCK);
+                        row_ok = false;
+                    }
+                }
+            }
+            // the 128-column scale blocks of B that this tile's columns fall in
+            constexpr int kSbPerTile = BN >= 128 ? BN / 128 : 1;
+            const float *sfb_g = sfb + static_cast<size_t>(ti.g) * NBs * KB;
+            const int nb0 = ti.n0 >> 7;
+            float sb_next[kSbPerTile];
+#pragma unroll
+            for (int i = 0; i < kSbPerTile; ++i)
+                sb_next[i] = __ldg(sfb_g + static_cast<size_t>(min(nb0 + i, NBs - 1)) * KB);
+
+            float acc[BN];
+#pragma unroll
+            for (int j = 0; j < BN; ++j)
+                acc[j] = 0.0f;
+
+            for (int kb = 0; kb < KB; ++kb) {
+                const uint32_t buf = tcount & 1u;
+                const uint32_t tph = (tcount >> 1) & 1u;
+                const bool got = wait_phase(tfull_bar(buf), tph, abort_flag, status) &&
+                                 wait_phase(full_bar(stage), phase, abort_flag, status);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                const float sa = sfa_smem[stage * kBM + r];
+                float sc[kSbPerTile];
+#pragma unroll
+                for (int i = 0; i < kSbPerTile; ++i) {
+                    sc[i] = sa * sb_next[i];   // fp32 product of the two scales, rounded once
+                    if (kb + 1 < KB)
+                        sb_next[i] = __ldg(sfb_g + static_cast<size_t>(min(nb0 + i, NBs - 1)) * KB + kb + 1);
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(empty_bar(stage));
+                tc_fence_after();
+                const uint32_t t_buf = t_lane + buf * BN;
+                uint32_t v0[32], v1[32];
+                tmem_ld32(t_buf, v0);
+                tmem_wait_ld32(v0);
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t(&cur)[32] = (c & 1) ? v1 : v0;
+                    uint32_t(&nxt)[32] = (c & 1) ? v0 : v1;
+                    if (c + 1 < BN / 32)
+                        tmem_ld32(t_buf + (c + 1) * 32, nxt);
+                    const float s = sc[(c * 32) / 128 < kSbPerTile ? (c * 32) / 128 : 0];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        acc[c * 32 + j] = fmaf(__uint_as_float(cur[j]), s, acc[c * 32 + j]);
+                    if (c + 1 < BN / 32)
+                        tmem_wait_ld32(nxt);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(tempty_bar(buf));
+                ++tcount;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok)
+                break;
+            if (row_ok) {
+                uint16_t *dst = d + d_row * p.N + ti.n0;
+#pragma unroll
+                for (int c = 0; c < BN / 8; ++c) {
+                    if (ti.n0 + c * 8 < p.N)
+                        st_global_v4(dst + c * 8, pack_bf16x2(acc[c * 8 + 0], acc[c * 8 + 1]),
+                                     pack_bf16x2(acc[c * 8 + 2], acc[c * 8 + 3]),
+                                     pack_bf16x2(acc[c * 8 + 4], acc[c * 8 + 5]),
+                                     pack_bf16x2(acc[c * 8 + 6], acc[c * 8 + 7]));
+                }
+            }
+        }
+    }
+
+    // ------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ----------------------------------------------------------------- host side
+struct Plan {
+    int bn;
+    int stages;
+    int num_tiles;
+    int grid;
+    int smem;
+};
+
+constexpr int kBN = 128;
+constexpr int kStages = 6;
+
+Plan make_plan(int layout, int M, int N, int K, int G, int num_sms)
+{
+    (void)K;
+    Plan pl;
+    pl.bn = kBN;
+    pl.stages = kStages;
+    pl.smem = SmemLayout<kBN, kStages>::kAlloc;
+    const int nblk = ceil_div(N, pl.bn);
+    if (layout == DG_LAYOUT_MASKED) {
+        pl.num_tiles = G * ceil_div(M, kBM) * nblk;
+        pl.grid = num_sms;   // fixed: the real tile count is only known on the device
+    } else {
+        pl.num_tiles = ceil_div(M, kBM) * nblk;
+        pl.grid = pl.num_tiles < num_sms ? pl.num_tiles : num_sms;
+    }
+    if (pl.grid < 1)
+        pl.grid = 1;
+    return pl;
+}
+
+dg_status_t check_common(const void *a, const void *sfa, const void *b, const void *sfb, const void *d, int M,
+                         int N, int K)
+{
+    if (!a || !sfa || !b || !sfb || !d || M <= 0 || N <= 0 || K <= 0)
+        return DG_ERR_INVALID_ARG;
+    if (K % kBK != 0 || N % 8 != 0)
+        return DG_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(d))
+        return DG_ERR_MISALIGNED;
+    return DG_OK;
+}
+
+dg_status_t launch(int layout, const uint8_t *a, const float *sfa, const uint8_t *b, const float *sfb, uint16_t *d,
+                   const int32_t *meta, int M, int N, int K, int G, void *stream)
+{
+    DeviceInfo info;
+    dg_status_t st = current_device(&info);
+    if (st != DG_OK)
+        return st;
+    const Plan pl = make_plan(layout, M, N, K, G, info.sm_count);
+    const int KB = K / kBK;
+    const int ldsfa = round_up(M, 4);
+
+    CUtensorMap ta, tb, ts;
+    {
+        // A: E4M3 [rows][K] (dense / contiguous) or [G][max_m][K] (masked)
+        const uint64_t dims3[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint64_t>(G)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(K) * M};
+        const uint32_t box[3] = {kBK, kBM, 1};
+        st = encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, layout == DG_LAYOUT_MASKED ? 3 : 2, a, dims3,
+                               strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != DG_OK)
+            return st;
+    }
+    {
+        // B: E4M3 [N][K] (dense) or [G][N][K]
+        const int Gb = layout == DG_LAYOUT_DENSE ? 1 : G;
+        const uint64_t dims3[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(Gb)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(K) * N};
+        const uint32_t box[3] = {kBK, static_cast<uint32_t>(pl.bn), 1};
+        st = encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, layout == DG_LAYOUT_DENSE ? 2 : 3, b, dims3,
+                               strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != DG_OK)
+            return st;
+    }
+    {
+        // SFA: fp32 [K/128][ldsfa] (dense / contiguous) or [G][K/128][ldsfa]
+        const uint64_t dims3[3] = {static_cast<uint64_t>(M), static_cast<uint64_t>(KB), static_cast<uint64_t>(G)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(ldsfa) * 4, static_cast<uint64_t>(ldsfa) * 4 * KB};
+        const uint32_t box[3] = {kBM, 1, 1};
+        st = encode_tensor_map(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, layout == DG_LAYOUT_MASKED ? 3 : 2, sfa, dims3,
+                               strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st != DG_OK)
+            return st;
+    }
+    auto kernel = fp8_gemm_kernel<kBN, kStages>;
+    st = ensure_smem_attr(reinterpret_cast<const void *>(kernel), pl.smem);
+    if (st != DG_OK)
+        return st;
+    Problem prob{M, N, K, G, layout};
+    kernel<<<pl.grid, kThreads, pl.smem, static_cast<cudaStream_t>(stream)>>>(ta, tb, ts, sfb, d, meta, prob,
+                                                                                info.status_word);
+    return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace dg
+
+extern "C" dg_status_t dg_fp8_gemm_nt(const uint8_t *a, const float *sfa, const uint8_t *b, const float *sfb,
+                                      uint16_t *d, int M, int N, int K, void *stream)
+{
+    dg_status_t st = dg::check_common(a, sfa, b, sfb, d, M, N, K);
+    if (st != DG_OK)
+        return st;
+    return dg::launch(DG_LAYOUT_DENSE, a, sfa, b, sfb, d, nullptr, M, N, K, 1, stream);
+}
+
+extern "C" dg_status_t dg_fp8_grouped_contiguous(const uint8_t *a, const float *sfa, const uint8_t *b,
+                                                 const float *sfb, uint16_t *d, const int32_t *m_indices,
+                                                 int sum_M, int N, int K, int G, void *stream)
+{
+    dg_status_t st = dg::check_common(a, sfa, b, sfb, d, sum_M, N, K);
+    if (st != DG_OK)
+        return st;
+    if (!m_indices || G <= 0)
+        return DG_ERR_INVALID_ARG;
+    if (sum_M % dg::kBM != 0)
+        return DG_ERR_UNSUPPORTED_SHAPE;
+    if (!dg::aligned16(m_indices))
+        return DG_ERR_MISALIGNED;
+    return dg::launch(DG_LAYOUT_CONTIGUOUS, a, sfa, b, sfb, d, m_indices, sum_M, N, K, G, stream);
+}
+
+extern "C" dg_status_t dg_fp8_grouped_masked(const uint8_t *a, const float *sfa, const uint8_t *b,
+                                             const float *sfb, uint16_t *d, const int32_t *masked_m, int G,
+                                             int max_m, int N, int K, int expected_m, void *stream)
+{
+    (void)expected_m;
+    dg_status_t st = dg::check_common(a, sfa, b, sfb, d, max_m, N, K);
+    if (st != DG_OK)
+        return st;
+    if (!masked_m || G <= 0)
+        return DG_ERR_INVALID_ARG;
+    if (G > dg::kMaxMaskedGroups)
+        return DG_ERR_UNSUPPORTED_SHAPE;
+    if (!dg::aligned16(masked_m))
+        return DG_ERR_MISALIGNED;
+    return dg::launch(DG_LAYOUT_MASKED, a, sfa, b, sfb, d, masked_m, max_m, N, K, G, stream);
+}
+
+extern "C" dg_status_t dg_query_plan(int layout, int M, int N, int K, int G, int num_sms, dg_plan_t *out)
+{
+    if (!out || M <= 0 || N <= 0 || K <= 0 || G <= 0 ||
+        (layout != DG_LAYOUT_DENSE && layout != DG_LAYOUT_CONTIGUOUS && layout != DG_LAYOUT_MASKED))
+        return DG_ERR_INVALID_ARG;
+    if (K % dg::kBK != 0 || N % 8 != 0)
+        return DG_ERR_UNSUPPORTED_SHAPE;
+    if (num_sms <= 0) {
+        dg::DeviceInfo info;
+        dg_status_t st = dg::current_device(&info);
+        if (st != DG_OK)
+            return st;
+        num_sms = info.sm_count;
+    }
+    const dg::Plan pl = dg::make_plan(layout, M, N, K, G, num_sms);
+    out->block_m = dg::kBM;
+    out->block_n = pl.bn;
+    out->stages = pl.stages;
+    out->num_tiles = pl.num_tiles;
+    out->grid = pl.grid;
+    out->smem_bytes = pl.smem;
+    return DG_OK;
+}

@@ -1,0 +1,196 @@
+// FP8 quantisers: per-token 1x128 groups for activations and 128x128 blocks
+// for weights ("DeepGEMM：一款支持FP8通用矩阵乘法(GEMM)的开源库", 功能特色/细粒度缩放功能;
+// 2kiu.com tutorial 4.4 精度控制与数值稳定性: scales from data statistics and
+// saturation of out-of-range values).
+//
+// Rule per group: amax = max|x|, s = max(amax, 1e-4f) / 448 (IEEE fp32
+// division), q = E4M3 RNE with saturation of fp32(x / s) (IEEE division).
+//
+// The activation quantiser is HBM-bound: 4 (or 2) bytes in and 1 + 4/128
+// bytes out per element.  One warp quantises one 128-value group with one
+// 16-byte load per lane; a block of 8 warps covers 8 consecutive rows x 4
+// consecutive groups so that each warp keeps 4 independent loads in flight and
+// the 8 scales of one group column land in one 32-byte sector.
+#include "dg_common.h"
+#include "dg_ptx.cuh"
+
+namespace dg {
+namespace {
+
+constexpr int kQuantWarps = 8;        // rows per block
+constexpr int kQuantGroupsPerWarp = 4;  // K-groups per warp
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
+{
+    uint16_t lo, hi;
+    // the first source lands in the upper byte of each pair
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float4 load_group4(const float *x, size_t off)
+{
+    return __ldcs(reinterpret_cast<const float4 *>(x + off));
+}
+
+__device__ __forceinline__ float4 load_group4(const uint16_t *x, size_t off)
+{
+    uint2 u = __ldcs(reinterpret_cast<const uint2 *>(x + off));
+    float4 f;
+    f.x = __uint_as_float(u.x << 16);
+    f.y = __uint_as_float(u.x & 0xFFFF0000u);
+    f.z = __uint_as_float(u.y << 16);
+    f.w = __uint_as_float(u.y & 0xFFFF0000u);
+    return f;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kQuantWarps * 32) quant_act_1x128_kernel(const T *__restrict__ x,
+                                                                          uint8_t *__restrict__ q,
+                                                                          float *__restrict__ sfa, int M, int K,
+                                                                          int ldsfa)
+{
+    const int KB = K / kQBlock;
+    const int row_tiles = (M + kQuantWarps - 1) / kQuantWarps;
+    const int col_tiles = (KB + kQuantGroupsPerWarp - 1) / kQuantGroupsPerWarp;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    for (int task = blockIdx.x; task < row_tiles * col_tiles; task += gridDim.x) {
+        const int m = (task / col_tiles) * kQuantWarps + warp;
+        const int kb0 = (task % col_tiles) * kQuantGroupsPerWarp;
+        if (m >= M)
+            continue;
+        float4 v[kQuantGroupsPerWarp];
+#pragma unroll
+        for (int j = 0; j < kQuantGroupsPerWarp; ++j)
+            if (kb0 + j < KB)
+                v[j] = load_group4(x, static_cast<size_t>(m) * K + static_cast<size_t>(kb0 + j) * kQBlock + lane * 4);
+#pragma unroll
+        for (int j = 0; j < kQuantGroupsPerWarp; ++j) {
+            const int kb = kb0 + j;
+            if (kb >= KB)
+                break;
+            float amax = fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w)));
+            amax = warp_max(amax);
+            const float s = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
+            const uint32_t packed = e4m3x4(__fdiv_rn(v[j].x, s), __fdiv_rn(v[j].y, s), __fdiv_rn(v[j].z, s),
+                                           __fdiv_rn(v[j].w, s));
+            __stcs(reinterpret_cast<uint32_t *>(q + static_cast<size_t>(m) * K + static_cast<size_t>(kb) * kQBlock) +
+                       lane,
+                   packed);
+            if (lane == 0)
+                sfa[static_cast<size_t>(kb) * ldsfa + m] = s;
+        }
+    }
+}
+
+// One block per (matrix g, 128-row block nb, 128-column block kb): 256 threads
+// hold the 16384 values in registers, reduce amax, then quantise.
+__global__ void __launch_bounds__(256) quant_weight_128x128_kernel(const float *__restrict__ w,
+                                                                   uint8_t *__restrict__ q,
+                                                                   float *__restrict__ sfb, int N, int K)
+{
+    const int KB = K / kQBlock;
+    const int NB = (N + kQBlock - 1) / kQBlock;
+    const int kb = blockIdx.x % KB;
+    const int nb = (blockIdx.x / KB) % NB;
+    const int g = blockIdx.x / (KB * NB);
+    const float *wg = w + static_cast<size_t>(g) * N * K;
+    uint8_t *qg = q + static_cast<size_t>(g) * N * K;
+    __shared__ float red[8];
+
+    float4 v[16];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int e = i * 256 + threadIdx.x;
+        const int n = nb * kQBlock + e / 32;
+        const int k = kb * kQBlock + (e % 32) * 4;
+        if (n < N) {
+            v[i] = *reinterpret_cast<const float4 *>(wg + static_cast<size_t>(n) * K + k);
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+        }
+    }
+    amax = warp_max(amax);
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i)
+        amax = fmaxf(amax, red[i]);
+    const float s = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int e = i * 256 + threadIdx.x;
+        const int n = nb * kQBlock + e / 32;
+        const int k = kb * kQBlock + (e % 32) * 4;
+        if (n < N)
+            *reinterpret_cast<uint32_t *>(qg + static_cast<size_t>(n) * K + k) =
+                e4m3x4(__fdiv_rn(v[i].x, s), __fdiv_rn(v[i].y, s), __fdiv_rn(v[i].z, s), __fdiv_rn(v[i].w, s));
+    }
+    if (threadIdx.x == 0)
+        sfb[(static_cast<size_t>(g) * NB + nb) * KB + kb] = s;
+}
+
+}  // namespace
+}  // namespace dg
+
+extern "C" dg_status_t dg_quant_act_1x128(const void *x, int x_dtype, uint8_t *q, float *sfa, int M, int K,
+                                          void *stream)
+{
+    using namespace dg;
+    if (!x || !q || !sfa || M <= 0 || K <= 0 || (x_dtype != DG_DTYPE_F32 && x_dtype != DG_DTYPE_BF16))
+        return DG_ERR_INVALID_ARG;
+    if (K % kQBlock != 0)
+        return DG_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(sfa))
+        return DG_ERR_MISALIGNED;
+    DeviceInfo info;
+    dg_status_t st = current_device(&info);
+    if (st != DG_OK)
+        return st;
+    const int KB = K / kQBlock;
+    const long long tasks = static_cast<long long>(ceil_div(M, kQuantWarps)) * ceil_div(KB, kQuantGroupsPerWarp);
+    const int grid = static_cast<int>(tasks < info.sm_count * 8LL ? tasks : info.sm_count * 8LL);
+    const int ldsfa = round_up(M, 4);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (x_dtype == DG_DTYPE_F32)
+        quant_act_1x128_kernel<float><<<grid, kQuantWarps * 32, 0, s>>>(static_cast<const float *>(x), q, sfa, M,
+                                                                         K, ldsfa);
+    else
+        quant_act_1x128_kernel<uint16_t><<<grid, kQuantWarps * 32, 0, s>>>(static_cast<const uint16_t *>(x), q,
+                                                                            sfa, M, K, ldsfa);
+    return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+}
+
+extern "C" dg_status_t dg_quant_weight_128x128(const float *w, uint8_t *q, float *sfb, int G, int N, int K,
+                                               void *stream)
+{
+    using namespace dg;
+    if (!w || !q || !sfb || G <= 0 || N <= 0 || K <= 0)
+        return DG_ERR_INVALID_ARG;
+    if (K % kQBlock != 0)
+        return DG_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(w) || !aligned16(q) || !aligned16(sfb))
+        return DG_ERR_MISALIGNED;
+    DeviceInfo info;
+    dg_status_t st = current_device(&info);
+    if (st != DG_OK)
+        return st;
+    const long long blocks = static_cast<long long>(G) * ceil_div(N, kQBlock) * (K / kQBlock);
+    if (blocks > 0x7FFFFFFFLL)
+        return DG_ERR_UNSUPPORTED_SHAPE;
+    quant_weight_128x128_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        w, q, sfb, N, K);
+    return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+}

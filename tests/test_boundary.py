@@ -1,0 +1,109 @@
+"""The C-ABI boundary without a GPU: the library builds for sm_103a, loads,
+exports every entry point include/dg.h declares, rejects bad arguments with
+the documented codes before touching the device, and plans tiles with the
+arithmetic the pages give."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import moe_grouped_gemm_x128_gb300 as dg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dg.build()
+    return dg.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "dg.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(dg_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_and_binding_agree():
+    assert declared_symbols() == sorted(dg.EXPORTED)
+
+
+def test_library_exports_every_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = dg.status_string(code)
+        assert isinstance(s, str) and s
+    assert dg.status_string(99) == "unknown status"
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def call(lib, name, *args):
+    return getattr(lib, name)(*args)
+
+
+def test_quant_validation(lib):
+    assert call(lib, "dg_quant_act_1x128", None, 0, FAKE, FAKE, 4, 128, None) == dg.DG_ERR_INVALID_ARG
+    assert call(lib, "dg_quant_act_1x128", FAKE, 7, FAKE, FAKE, 4, 128, None) == dg.DG_ERR_INVALID_ARG
+    assert call(lib, "dg_quant_act_1x128", FAKE, 0, FAKE, FAKE, 0, 128, None) == dg.DG_ERR_INVALID_ARG
+    assert call(lib, "dg_quant_act_1x128", FAKE, 0, FAKE, FAKE, 4, 100, None) == dg.DG_ERR_UNSUPPORTED_SHAPE
+    assert call(lib, "dg_quant_act_1x128", FAKE + 4, 0, FAKE, FAKE, 4, 128, None) == dg.DG_ERR_MISALIGNED
+    assert call(lib, "dg_quant_weight_128x128", FAKE, FAKE, None, 1, 128, 128, None) == dg.DG_ERR_INVALID_ARG
+    assert call(lib, "dg_quant_weight_128x128", FAKE, FAKE, FAKE, 1, 128, 130, None) == dg.DG_ERR_UNSUPPORTED_SHAPE
+
+
+def test_gemm_validation(lib):
+    F = FAKE
+    assert call(lib, "dg_fp8_gemm_nt", F, F, F, F, None, 128, 256, 512, None) == dg.DG_ERR_INVALID_ARG
+    assert call(lib, "dg_fp8_gemm_nt", F, F, F, F, F, -1, 256, 512, None) == dg.DG_ERR_INVALID_ARG
+    assert call(lib, "dg_fp8_gemm_nt", F, F, F, F, F, 128, 256, 500, None) == dg.DG_ERR_UNSUPPORTED_SHAPE
+    assert call(lib, "dg_fp8_gemm_nt", F, F, F, F, F, 128, 252, 512, None) == dg.DG_ERR_UNSUPPORTED_SHAPE
+    assert call(lib, "dg_fp8_gemm_nt", F, F + 8, F, F, F, 128, 256, 512, None) == dg.DG_ERR_MISALIGNED
+    # contiguous: sum_M must be a multiple of 128, G > 0, m_indices non-null
+    assert call(lib, "dg_fp8_grouped_contiguous", F, F, F, F, F, F, 200, 256, 512, 2, None) == \
+        dg.DG_ERR_UNSUPPORTED_SHAPE
+    assert call(lib, "dg_fp8_grouped_contiguous", F, F, F, F, F, None, 256, 256, 512, 2, None) == \
+        dg.DG_ERR_INVALID_ARG
+    assert call(lib, "dg_fp8_grouped_contiguous", F, F, F, F, F, F, 256, 256, 512, 0, None) == \
+        dg.DG_ERR_INVALID_ARG
+    # masked: G limit and alignment of masked_m
+    assert call(lib, "dg_fp8_grouped_masked", F, F, F, F, F, F, 5000, 256, 256, 512, 0, None) == \
+        dg.DG_ERR_UNSUPPORTED_SHAPE
+    assert call(lib, "dg_fp8_grouped_masked", F, F, F, F, F, F + 4, 4, 256, 256, 512, 0, None) == \
+        dg.DG_ERR_MISALIGNED
+    assert call(lib, "dg_fp8_grouped_masked", F, F, F, F, F, F, 4, 0, 256, 512, 0, None) == dg.DG_ERR_INVALID_ARG
+
+
+def test_read_status_validation(lib):
+    assert lib.dg_read_device_status(None, None) == dg.DG_ERR_INVALID_ARG
+
+
+def test_plan_tile_arithmetic_of_the_pages():
+    # M=256, N=7168: 128-wide blocks give 2 x 56 = 112 tiles (the page's
+    # "112 compute units"); the 112-wide alternative would give 2 x 64 = 128.
+    p = dg.dg_query_plan(dg.DG_LAYOUT_DENSE, 256, 7168, 2048, 1, num_sms=132)
+    assert p["block_m"] == 128
+    assert p["num_tiles"] == (256 // p["block_m"]) * (-(-7168 // p["block_n"]))
+    if p["block_n"] == 128:
+        assert p["num_tiles"] == 112
+    assert 2 * (7168 // 112) == 128
+
+
+def test_plan_shapes():
+    for (M, N, K) in [(128, 256, 512), (4096, 7168, 18432), (4096, 24576, 1536), (4096, 2112, 7168), (1, 8, 128)]:
+        p = dg.dg_query_plan(dg.DG_LAYOUT_DENSE, M, N, K, 1, num_sms=152)
+        tiles = -(-M // p["block_m"]) * -(-N // p["block_n"])
+        assert p["num_tiles"] == tiles
+        assert p["grid"] == min(tiles, 152)
+        assert p["smem_bytes"] <= 232448
+    # masked: fixed grid = SM count (the real tile count lives on the device)
+    p = dg.dg_query_plan(dg.DG_LAYOUT_MASKED, 256, 7168, 2048, 16, num_sms=152)
+    assert p["grid"] == 152
+    assert p["num_tiles"] == 16 * 2 * -(-7168 // p["block_n"])
+    with pytest.raises(dg.DgError):
+        dg.dg_query_plan(dg.DG_LAYOUT_DENSE, 128, 256, 100, 1, num_sms=152)
