@@ -39,10 +39,12 @@ L2_BYTES = 129 * 2 ** 20
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="dg", choices=["dg", "reference"])
     ap.add_argument("--workload", default="skinny", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--shape", default="", help="M,N,K: a dense problem of this shape instead of the workload "
+                                                 "(profiling aid; not a bench line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
@@ -152,48 +154,73 @@ def algorithmic_bytes(w: wl.Workload):
 
 # ---------------------------------------------------------------- CPU leg --
 def cpu_oracle_rate(w: wl.Workload, seconds: float):
-    """Time the oracle (quantise + GEMM) on whole rows of the workload until
-    about `seconds` have passed; returns (TFLOP/s, rows, elapsed, threads)."""
+    """Time the oracle (quantise + GEMM) over whole rows of the workload,
+    repeating the full row range until about `seconds` have passed; returns
+    (TFLOP/s, rows computed, elapsed s, threads)."""
     import oracle
     if w.layout != "dense":
         raise SystemExit("the CPU baseline leg covers the dense workloads")
     x, wt = wl.dense_inputs(w.M, w.N, w.K, w.seed, w.outliers)
     qb, sfb = oracle.quant_weight_128x128(wt)
-    rows_done, elapsed, chunk = 0, 0.0, 8
-    while elapsed < seconds and rows_done < w.M:
-        r1 = min(w.M, rows_done + chunk)
+    rows_done, elapsed, chunk, r0 = 0, 0.0, 8, 0
+    while elapsed < seconds:
+        r1 = min(w.M, r0 + chunk)
         t0 = time.perf_counter()
-        qa, sfa = oracle.quant_act_1x128(x[rows_done:r1])
+        qa, sfa = oracle.quant_act_1x128(x[r0:r1])
         oracle.gemm_nt(qa, sfa, qb, sfb)
         elapsed += time.perf_counter() - t0
-        rows_done = r1
+        rows_done += r1 - r0
+        r0 = 0 if r1 >= w.M else r1
         chunk = min(chunk * 2, 64)
     flops = 2.0 * rows_done * w.N * w.K
     return flops / elapsed / 1e12, rows_done, elapsed, oracle.num_threads()
 
 
 def run_reference(args, w):
+    """The oracle as it stands, timed on the host cores: every step quantises
+    and multiplies a bounded sample of the workload (up to one row per oracle
+    thread, and as many output columns as fit the per-step share of a two
+    minute budget); the value is the sampled FLOPs over the sampled time."""
+    import oracle
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    rates = []
-    rows = 0
-    per_step = max(1.0, args.cpu_seconds / max(args.steps, 1))
+    if w.layout != "dense":
+        raise SystemExit("the CPU reference arm covers the dense workloads")
+    x, wt = wl.dense_inputs(w.M, w.N, w.K, w.seed, w.outliers)
+    qb, sfb = oracle.quant_weight_128x128(wt)
+    thr = oracle.num_threads()
+    rows = min(w.M, thr)
+    per_step = 120.0 / (args.steps + args.warmup)
+    # calibrate the output-element rate on one 128-column slice
+    t0 = time.perf_counter()
+    qa, sfa = oracle.quant_act_1x128(x[:rows])
+    oracle.gemm_nt(qa, sfa, qb[:128], sfb[:1])
+    rate = rows * 128 / max(time.perf_counter() - t0, 1e-6)
+    cols = int(max(8, min(w.N, rate * per_step / rows)) // 8 * 8)
+    nbs = -(-cols // 128)
+    flops = 0.0
+    elapsed = 0.0
     for i in range(args.warmup + args.steps):
-        rate, rows, el, thr = cpu_oracle_rate(w, per_step if i >= args.warmup else 0.2)
+        r0 = (i * rows) % w.M
+        xr = x[r0:r0 + rows]
+        t0 = time.perf_counter()
+        qa, sfa = oracle.quant_act_1x128(xr)
+        oracle.gemm_nt(qa, sfa, np.ascontiguousarray(qb[:cols]), np.ascontiguousarray(sfb[:nbs]))
+        dt = time.perf_counter() - t0
         if i >= args.warmup:
-            rates.append(rate)
-    value = statistics.mean(rates)
+            elapsed += dt
+            flops += 2.0 * len(xr) * cols * w.K
+    value = flops / elapsed / 1e12
     rows_total = gemm_shape(w)[0]
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 2.0 * gemm_shape(w)[1] * w.N * w.K / (value * 1e12) * 1e3,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 block sums, fp32 promotion",
         "data": "synthetic", "config": {"workload": describe(w)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
-                         "sample": f"first {rows} of {rows_total} rows per step (quantise + GEMM), "
-                                   f"rate scaled to the full workload"},
+                         "sample": f"per step {rows} of {rows_total} rows x {cols} of {w.N} columns "
+                                   f"(quantise + GEMM), {elapsed:.1f} s timed"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -237,33 +264,64 @@ def run_gpu(args, w):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
-    def step(i, ev=None):
+    def quant(i):
         j = i % n_sets
         dg.dg_quant_act_1x128(xs[j], qas[j], sfas[j])
-        if ev is not None:
-            ev.record(stream)
+
+    def gemm(i):
+        j = i % n_sets
         dg.dg_fp8_gemm_nt(qas[j], sfas[j], qbs[j], sfbs[j], ds[j])
+
+    def step(i):
+        quant(i)
+        gemm(i)
 
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
 
-    # timed region: K steps; events split each step into quantiser | GEMM
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps + 1)]
+    # The steps are launched from a CUDA graph (host launch cost would
+    # otherwise dominate microsecond kernels): one graph holds `chunk` steps
+    # over the rotating input sets and is replayed until `steps` steps have run.
+    chunk = min(args.steps, 100)
+    reps = -(-args.steps // chunk)
+    steps_run = chunk * reps
+
+    def capture(body):
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for i in range(chunk):
+                body(i)
+        g.replay()
+        torch.cuda.synchronize()
+        return g
+
+    def timed(graph, n):
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for _ in range(n):
+            graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
+
+    g_step = capture(step)
+    g_gemm = capture(gemm)
+    g_quant = capture(quant)
     with ClockSampler(local) as clk:
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
-        ev[0].record(stream)
-        for i in range(args.steps):
-            step(i, ev[2 * i + 1])
-            ev[2 * i + 2].record(stream)
-        torch.cuda.synchronize()
+        total_ms = timed(g_step, reps)
         if world > 1:
             dist.barrier()
-    total_ms = ev[0].elapsed_time(ev[-1])
-    quant_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps))
-    gemm_ms = sum(ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(args.steps))
+    # per-kernel durations: the same launches, one kernel kind per graph
+    gemm_ms = timed(g_gemm, reps)
+    quant_ms = timed(g_quant, reps)
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -276,10 +334,12 @@ def run_gpu(args, w):
         xs[0].copy_(x_pin, non_blocking=True)
         step(0)
         d_pin.copy_(ds[0], non_blocking=True)
+    # (the end-to-end loop calls the API directly, one launch per kernel)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = min(args.steps, 500)
     e0.record(stream)
-    for i in range(args.steps):
+    for i in range(e2e_steps):
         j = i % n_sets
         xs[j].copy_(x_pin, non_blocking=True)
         step(i)
@@ -289,12 +349,12 @@ def run_gpu(args, w):
     e2e_ms = e0.elapsed_time(e1)
 
     flops_step = 2.0 * M * N * K
-    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
-    e2e_value = world * flops_step * args.steps / (e2e_ms * 1e-3) / 1e12
+    value = world * flops_step * steps_run / (total_ms * 1e-3) / 1e12
+    e2e_value = world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
 
     hbm, bf16, bf16_sus, src = peaks()
     fp8_peak = bf16 * FP8_PER_BF16
-    gemm_s = gemm_ms / args.steps * 1e-3
+    gemm_s = gemm_ms / steps_run * 1e-3
     ab = algorithmic_bytes(w)
     t_mem = ab / (hbm * 1e9)
     t_cmp = flops_step / (fp8_peak * 1e12)
@@ -308,26 +368,28 @@ def run_gpu(args, w):
         else "fallback"
     roof["kernel"] = "fp8_gemm_kernel"
     roof["kernel_us"] = gemm_s * 1e6
-    roof["quant_us"] = quant_ms / args.steps * 1e3
+    roof["quant_us"] = quant_ms / steps_run * 1e3
     roof["algorithmic_bytes"] = ab
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps_run,
+        "warmup": args.warmup, "ms_per_step": total_ms / steps_run, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
         "config": {"workload": describe(w), "l2": f"rotating {n_sets} input sets of {set_bytes / 1e6:.1f} MB "
                                                   f"(> 2x L2) between steps",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": M * K * 4, "d2h_bytes_per_step": M * N * 2},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 2 * steps_run,
+        "launch": f"CUDA graph of {chunk} steps replayed {reps} times; kernel times from graphs of the same "
+                  f"launches of one kernel",
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, rows, el, thr = cpu_oracle_rate(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": thr, "kind": "oracle",
-                                "sample": f"oracle quantise + GEMM on the first {rows} of {M} rows "
-                                          f"({el:.1f} s), rate scaled to TFLOP/s"}
+                                "sample": f"oracle quantise + GEMM over {rows} rows of the {M}-row workload "
+                                          f"(row range repeated, {el:.1f} s of CPU time), rate in TFLOP/s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -337,6 +399,9 @@ def run_gpu(args, w):
 def main():
     args = parse()
     w = wl.WORKLOADS[args.workload]
+    if args.shape:
+        M, N, K = (int(v) for v in args.shape.split(","))
+        w = wl.Workload(f"shape_{M}x{N}x{K}", "dense", M=M, N=N, K=K, seed=5)
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -9,20 +9,26 @@
 // kb ascending; D = bf16_rn(acc).
 //
 // How (the page's 线程专业化技术 and 统一的计算任务调度系统, redone for GB300):
-// a persistent kernel, one CTA per SM, 256 threads in four roles:
+// a persistent kernel, one CTA per SM, 384 threads in four roles:
 //   warp 0      TMA producer: streams A[128x128], B[BNx128] (128-byte swizzled)
 //               and the 128 SFA scales of each K block into an S-stage ring;
 //   warp 1      MMA issuer: one thread issues 4 x tcgen05.mma kind::f8f6f4
-//               (128 x BN x 32) per K block into one of two TMEM partial
-//               buffers (the first with accumulate off, so each K block starts
-//               from zero), then commits to the ring's "empty" barrier and the
-//               buffer's "full" barrier;
+//               (128 x BN x 32) per K block into one of up to four TMEM
+//               partial buffers (the first with accumulate off, so each K
+//               block starts from zero), then commits to the ring's "empty"
+//               barrier and the buffer's "full" barrier;
 //   warp 2      allocates / frees the TMEM columns;
-//   warps 4-7   epilogue: each thread owns one output row (TMEM lane); per K
-//               block it loads the partial row from TMEM, scales and FMAs it
-//               into fp32 registers, and releases the buffer, so the MMA of
-//               block kb+1 overlaps the promotion of block kb; after the last
-//               block it converts to bf16 and stores the row.
+//   warp 3      (masked layout) builds the per-expert tile prefix;
+//   warps 4-11  epilogue, two warpgroups each owning half of the tile's
+//               columns: each thread owns one output row (TMEM lane); per K
+//               block it loads its partial row from TMEM, scales it and FMAs it
+//               into fp32 registers (two lanes per instruction), and releases
+//               the buffer, so the MMAs of the next K blocks overlap the
+//               promotion of this one; after the last block it converts to
+//               bf16 and stores the row.
+// The kernel is launched as a programmatic dependent of the previous kernel in
+// the stream: its prologue (barriers, TMEM, descriptor prefetch) overlaps that
+// kernel's tail, and every thread waits for it before touching global memory.
 // Tiles are visited in a grouped order (GROUP_M m-blocks per band) so that the
 // CTAs running at the same time share A and B tiles through L2.
 //
@@ -38,9 +44,10 @@ namespace {
 constexpr int kBM = 128;                   // rows per tile (tcgen05 M)
 constexpr int kBK = 128;                   // K per stage = one promotion block = one 128-byte row
 constexpr int kMmaK = 32;                  // K per tcgen05.mma for 8-bit inputs
-constexpr int kThreads = 256;
 constexpr int kEpiWarp0 = 4;
-constexpr int kNumEpiWarps = 4;
+constexpr int kEpiGroups = 2;                       // epilogue warpgroups
+constexpr int kNumEpiWarps = 4 * kEpiGroups;
+constexpr int kThreads = 32 * (kEpiWarp0 + kNumEpiWarps);   // 384
 constexpr int kGroupM = 16;                // m-blocks per rasterisation band
 constexpr int kMaxMaskedGroups = 1024;     // G limit of the masked layout (tile prefix in smem)
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
@@ -54,8 +61,8 @@ struct SmemLayout {
     static constexpr int kBOff = kAOff + STAGES * kABytes;
     static constexpr int kSfaOff = kBOff + STAGES * kBBytes;
     static constexpr int kBarOff = kSfaOff + STAGES * kSfaBytes;
-    // full[S], empty[S], tfull[2], tempty[2], drain
-    static constexpr int kNumBars = 2 * STAGES + 5;
+    // full[S], empty[S], tfull[4], tempty[4], drain
+    static constexpr int kNumBars = 2 * STAGES + 9;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;   // tmem base, abort flag
     static constexpr int kPrefixOff = kMiscOff + 16;
     static constexpr int kBytes = kPrefixOff + (kMaxMaskedGroups + 1) * 4;
@@ -178,13 +185,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     unsigned int *status)
 {
     using L = SmemLayout<BN, STAGES>;
-    constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
-                                   : (2 * BN <= 256)                     ? 256
-                                                                         : 512;
+    // TMEM partial buffers: as many 128 x BN fp32 buffers as fit (max 4)
+    constexpr int kBufs = (4 * BN <= 512) ? 4 : (512 / BN);
+    constexpr uint32_t kTmemCols = (kBufs * BN <= 32)    ? 32
+                                   : (kBufs * BN <= 64)  ? 64
+                                   : (kBufs * BN <= 128) ? 128
+                                   : (kBufs * BN <= 256) ? 256
+                                                         : 512;
+    constexpr int kCols = BN / kEpiGroups;             // columns per epilogue warpgroup
+    constexpr int kChunks = kCols / 32;                // 32-column TMEM loads per K block
     constexpr uint32_t kStageTx = L::kABytes + L::kBBytes + L::kSfaBytes;
     constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, BN);
-    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 32 in [32, 256]");
-    static_assert(BN % 128 == 0 || 128 % BN == 0, "a 32-column chunk must not straddle two 128-column scale blocks");
+    static_assert(kCols % 32 == 0 && BN <= 256, "BN must be a multiple of 64 up to 256");
+    static_assert(kCols % 128 == 0 || 128 % kCols == 0,
+                  "the columns of one epilogue warpgroup must lie in one 128-column scale block");
+    static_assert(kBufs >= 2, "at least two TMEM partial buffers");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -193,8 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 4 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 8);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::kMiscOff + 4);
     int *prefix = reinterpret_cast<int *>(smem + L::kPrefixOff);
@@ -205,13 +220,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int KB = p.K / kBK;
     const int NBs = (p.N + 127) / 128;   // 128-column scale blocks of B
 
-    // ---------------------------------------------------------------- setup
+    // --------------------------------------------- setup (no global memory)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1 + kNumEpiWarps);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kBufs; ++b) {
             mbar_init(tfull_bar(b), 1);
             mbar_init(tempty_bar(b), kNumEpiWarps);
         }
@@ -219,11 +234,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_mbarrier_init();
         fence_proxy_async_smem();
+        tma_prefetch_desc(&tmap_a);
+        tma_prefetch_desc(&tmap_b);
+        tma_prefetch_desc(&tmap_sfa);
     }
     if (warp == 2) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
+    // the previous kernel in the stream may still be running until here
+    griddep_wait();
+
     Sched<BN> sch;
     sch.n_blocks = (p.N + BN - 1) / BN;
     sch.G = p.G;
@@ -271,9 +292,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            tma_prefetch_desc(&tmap_a);
-            tma_prefetch_desc(&tmap_b);
-            tma_prefetch_desc(&tmap_sfa);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t pending = 0;        // stages with a copy whose consumption was not yet observed
@@ -328,15 +346,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t tcount = 0;
+            int buf = 0;
+            uint32_t tph = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < sch.num_tiles; t += gridDim.x) {
                 const TileInfo ti = sch.tile(t, p, meta);
                 if (ti.skip)
                     continue;
                 for (int kb = 0; kb < KB; ++kb) {
-                    const uint32_t buf = tcount & 1u;
-                    const uint32_t tph = (tcount >> 1) & 1u;
                     if (!wait_phase(tempty_bar(buf), tph ^ 1u, abort_flag, status) ||
                         !wait_phase(full_bar(stage), phase, abort_flag, status)) {
                         ok = false;
@@ -352,7 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    kIdesc, k > 0 ? 1u : 0u);
                     mma_commit(empty_bar(stage));
                     mma_commit(tfull_bar(buf));
-                    ++tcount;
+                    if (++buf == kBufs) {
+                        buf = 0;
+                        tph ^= 1u;
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -365,12 +385,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kEpiWarp0) {
         // ---------------------------------------------------------- epilogue
-        const int q = warp & 3;                 // TMEM lane quarter of this warp
-        const int r = q * 32 + lane;            // row of the tile owned by this thread
-        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        const int q = warp & 3;                          // TMEM lane quarter of this warp
+        const int grp = (warp - kEpiWarp0) >> 2;         // column half of this warpgroup
+        const int r = q * 32 + lane;                     // row of the tile owned by this thread
+        const int c0 = grp * kCols;                      // first column of this warpgroup
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c0;
         int stage = 0;
         uint32_t phase = 0;
-        uint32_t tcount = 0;
+        int buf = 0;
+        uint32_t tph = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < sch.num_tiles; t += gridDim.x) {
             const TileInfo ti = sch.tile(t, p, meta);
@@ -395,37 +418,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // the 128-column scale blocks of B that this tile's columns fall in
-            constexpr int kSbPerTile = BN >= 128 ? BN / 128 : 1;
-            const float *sfb_g = sfb + static_cast<size_t>(ti.g) * NBs * KB;
-            const int nb0 = ti.n0 >> 7;
-            float sb_next[kSbPerTile];
-#pragma unroll
-            for (int i = 0; i < kSbPerTile; ++i)
-                sb_next[i] = __ldg(sfb_g + static_cast<size_t>(min(nb0 + i, NBs - 1)) * KB);
+            // the 128-column scale block of B holding this warpgroup's columns
+            const int nb = min((ti.n0 + c0) >> 7, NBs - 1);
+            const float *sfb_row = sfb + (static_cast<size_t>(ti.g) * NBs + nb) * KB;
+            float sb_next = __ldg(sfb_row);
 
-            float acc[BN];
+            float2 acc[kCols / 2];
 #pragma unroll
-            for (int j = 0; j < BN; ++j)
-                acc[j] = 0.0f;
+            for (int j = 0; j < kCols / 2; ++j)
+                acc[j] = make_float2(0.0f, 0.0f);
 
             for (int kb = 0; kb < KB; ++kb) {
-                const uint32_t buf = tcount & 1u;
-                const uint32_t tph = (tcount >> 1) & 1u;
                 const bool got = wait_phase(tfull_bar(buf), tph, abort_flag, status) &&
                                  wait_phase(full_bar(stage), phase, abort_flag, status);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
                 }
-                const float sa = sfa_smem[stage * kBM + r];
-                float sc[kSbPerTile];
-#pragma unroll
-                for (int i = 0; i < kSbPerTile; ++i) {
-                    sc[i] = sa * sb_next[i];   // fp32 product of the two scales, rounded once
-                    if (kb + 1 < KB)
-                        sb_next[i] = __ldg(sfb_g + static_cast<size_t>(min(nb0 + i, NBs - 1)) * KB + kb + 1);
-                }
+                // fp32 product of the two scales, rounded once
+                const float s = sfa_smem[stage * kBM + r] * sb_next;
+                const float2 s2 = make_float2(s, s);
+                if (kb + 1 < KB)
+                    sb_next = __ldg(sfb_row + kb + 1);
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(empty_bar(stage));
@@ -435,23 +449,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(t_buf, v0);
                 tmem_wait_ld32(v0);
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = 0; c < kChunks; ++c) {
                     uint32_t(&cur)[32] = (c & 1) ? v1 : v0;
                     uint32_t(&nxt)[32] = (c & 1) ? v0 : v1;
-                    if (c + 1 < BN / 32)
+                    if (c + 1 < kChunks)
                         tmem_ld32(t_buf + (c + 1) * 32, nxt);
-                    const float s = sc[(c * 32) / 128 < kSbPerTile ? (c * 32) / 128 : 0];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        acc[c * 32 + j] = fmaf(__uint_as_float(cur[j]), s, acc[c * 32 + j]);
-                    if (c + 1 < BN / 32)
+                    for (int j = 0; j < 16; ++j)
+                        acc[c * 16 + j] =
+                            ffma2(make_float2(__uint_as_float(cur[2 * j]), __uint_as_float(cur[2 * j + 1])), s2,
+                                  acc[c * 16 + j]);
+                    if (c + 1 < kChunks)
                         tmem_wait_ld32(nxt);
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(tempty_bar(buf));
-                ++tcount;
+                if (++buf == kBufs) {
+                    buf = 0;
+                    tph ^= 1u;
+                }
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
@@ -460,14 +478,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok)
                 break;
             if (row_ok) {
-                uint16_t *dst = d + d_row * p.N + ti.n0;
+                uint16_t *dst = d + d_row * p.N + ti.n0 + c0;
 #pragma unroll
-                for (int c = 0; c < BN / 8; ++c) {
-                    if (ti.n0 + c * 8 < p.N)
-                        st_global_v4(dst + c * 8, pack_bf16x2(acc[c * 8 + 0], acc[c * 8 + 1]),
-                                     pack_bf16x2(acc[c * 8 + 2], acc[c * 8 + 3]),
-                                     pack_bf16x2(acc[c * 8 + 4], acc[c * 8 + 5]),
-                                     pack_bf16x2(acc[c * 8 + 6], acc[c * 8 + 7]));
+                for (int c = 0; c < kCols / 8; ++c) {
+                    if (ti.n0 + c0 + c * 8 < p.N)
+                        st_global_v4(dst + c * 8, pack_bf16x2(acc[c * 4 + 0].x, acc[c * 4 + 0].y),
+                                     pack_bf16x2(acc[c * 4 + 1].x, acc[c * 4 + 1].y),
+                                     pack_bf16x2(acc[c * 4 + 2].x, acc[c * 4 + 2].y),
+                                     pack_bf16x2(acc[c * 4 + 3].x, acc[c * 4 + 3].y));
                 }
             }
         }
@@ -574,8 +592,18 @@ dg_status_t launch(int layout, const uint8_t *a, const float *sfa, const uint8_t
     if (st != DG_OK)
         return st;
     Problem prob{M, N, K, G, layout};
-    kernel<<<pl.grid, kThreads, pl.smem, static_cast<cudaStream_t>(stream)>>>(ta, tb, ts, sfb, d, meta, prob,
-                                                                                info.status_word);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pl.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, ts, sfb, d, meta, prob, info.status_word) != cudaSuccess)
+        return DG_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }
 

@@ -28,6 +28,22 @@ __device__ __forceinline__ uint32_t lane_id()
     return l;
 }
 
+// ------------------------------------------------- dependent launches ---
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialisation attribute may start before the previous kernel in the
+// stream has finished; griddep_wait blocks until that kernel has completed and
+// its memory is visible.  griddep_launch_dependents lets the next kernel start
+// launching early.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // -------------------------------------------------------------- mbarrier ---
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
@@ -205,6 +221,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr)
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N)
 {
     return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// d = a * b + c on two fp32 lanes at once (round to nearest even per lane,
+// the same result as two fmaf calls).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
 }
 
 // ------------------------------------------------------------- epilogue ---

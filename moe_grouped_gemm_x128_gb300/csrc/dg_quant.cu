@@ -64,6 +64,9 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quant_act_1x128_kernel(const
     const int col_tiles = (KB + kQuantGroupsPerWarp - 1) / kQuantGroupsPerWarp;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // a GEMM launched after this kernel may start its prologue now; it waits
+    // for this grid's completion before reading q or sfa
+    griddep_launch_dependents();
     for (int task = blockIdx.x; task < row_tiles * col_tiles; task += gridDim.x) {
         const int m = (task / col_tiles) * kQuantWarps + warp;
         const int kb0 = (task % col_tiles) * kQuantGroupsPerWarp;
