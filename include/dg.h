@@ -140,7 +140,10 @@ dg_status_t dg_fp8_grouped_masked(const uint8_t *a, const float *sfa, const uint
 /* Host-only: the tile plan the GEMM entry points would launch for this
  * problem on a GPU with `num_sms` SMs (num_sms <= 0: the current device's).
  * Makes no CUDA call when num_sms > 0.  For DG_LAYOUT_DENSE, M is the row
- * count; CONTIGUOUS: M = sum_M; MASKED: M = max_m. */
+ * count; CONTIGUOUS: M = sum_M; MASKED: M = max_m.  Tiles are 128 x 192 when
+ * the problem has at least one full wave of them, else 128 x 128; the
+ * environment variable DG_FORCE_BN=128|192 (read at every call) pins the
+ * width.  Results do not depend on the tile width. */
 dg_status_t dg_query_plan(int layout, int M, int N, int K, int G, int num_sms, dg_plan_t *out);
 
 /* Human-readable name of a status code (static string, never NULL). */

@@ -9,32 +9,36 @@
 // kb ascending; D = bf16_rn(acc).
 //
 // How (the page's 线程专业化技术 and 统一的计算任务调度系统, redone for GB300):
-// a persistent kernel, one CTA per SM, 384 threads in four roles:
-//   warp 0      TMA producer: streams A[128x128], B[BNx128] (128-byte swizzled)
-//               and the 128 SFA scales of each K block into an S-stage ring;
-//   warp 1      MMA issuer: one thread issues 4 x tcgen05.mma kind::f8f6f4
-//               (128 x BN x 32) per K block into one of up to four TMEM
-//               partial buffers (the first with accumulate off, so each K
-//               block starts from zero), then commits to the ring's "empty"
-//               barrier and the buffer's "full" barrier;
-//   warp 2      allocates / frees the TMEM columns;
-//   warp 3      (masked layout) builds the per-expert tile prefix;
-//   warps 4-11  epilogue, two warpgroups each owning half of the tile's
-//               columns: each thread owns one output row (TMEM lane); per K
-//               block it loads its partial row from TMEM, scales it and FMAs it
-//               into fp32 registers (two lanes per instruction), and releases
-//               the buffer, so the MMAs of the next K blocks overlap the
-//               promotion of this one; after the last block it converts to
+// a persistent kernel, one CTA per SM, 384 threads in three roles:
+//   warp 0      TMA producer: streams A[128x128] and B[BNx128] (128-byte
+//               swizzled) into an S-stage shared-memory ring; also allocates
+//               and frees the TMEM columns;
+//   warps 1, 2  MMA issuers, taking alternate K blocks: one thread each issues
+//               4 x tcgen05.mma kind::f8f6f4 (128 x BN x 32) per K block into
+//               a TMEM partial buffer (the first with accumulate off, so each
+//               K block starts from zero), then commits to the ring's "empty"
+//               barrier and the buffer's "full" barrier; two issuers let one's
+//               barrier round trips overlap the other's MMAs; warp 1 also
+//               builds the masked layout's per-expert tile prefix;
+//   warps 4-11  epilogue, two warpgroups each owning half of the
+//               tile's columns: each thread owns one output row (TMEM lane);
+//               per K block it loads its partial row from TMEM, scales it by
+//               sfa * sfb (read from global memory a few K blocks ahead) and
+//               FMAs it into fp32 registers (two lanes per instruction), then
+//               releases the buffer, so the MMAs of the next K blocks overlap
+//               the promotion of this one; after the last block it converts to
 //               bf16 and stores the row.
-// The kernel is launched as a programmatic dependent of the previous kernel in
-// the stream: its prologue (barriers, TMEM, descriptor prefetch) overlaps that
-// kernel's tail, and every thread waits for it before touching global memory.
+// Tiles are 128 x 192 (two TMEM buffers, three epilogue warpgroups, 512
+// threads) when the problem has at least a full wave of them, else 128 x 128
+// (four buffers, two epilogue warpgroups, 384 threads).
 // Tiles are visited in a grouped order (GROUP_M m-blocks per band) so that the
 // CTAs running at the same time share A and B tiles through L2.
 //
 // Every wait is bounded: after kWaitTimeoutNs a role raises the CTA's abort
 // flag and DG_DEVFLAG_TIMEOUT, the producer waits (bounded) for its own copies
 // in flight, the MMA thread drains its MMAs, TMEM is freed and the CTA exits.
+#include <stdlib.h>
+
 #include "dg_common.h"
 #include "dg_ptx.cuh"
 
@@ -43,11 +47,18 @@ namespace {
 
 constexpr int kBM = 128;                   // rows per tile (tcgen05 M)
 constexpr int kBK = 128;                   // K per stage = one promotion block = one 128-byte row
-constexpr int kMmaK = 32;                  // K per tcgen05.mma for 8-bit inputs
-constexpr int kEpiWarp0 = 4;
-constexpr int kEpiGroups = 2;                       // epilogue warpgroups
-constexpr int kNumEpiWarps = 4 * kEpiGroups;
-constexpr int kThreads = 32 * (kEpiWarp0 + kNumEpiWarps);   // 384
+constexpr int kEpiWarp0 = 4;                        // warps 0-3: producer, two MMA issuers, spare
+constexpr int kEpiCols = 64;                        // tile columns per epilogue warpgroup
+constexpr int kIssuers = 2;                         // MMA-issuing threads (warps 1 and 2)
+
+// Threads of the CTA for a tile width: 4 warps + one warpgroup per 64 columns
+// (BN = 128: 384 threads, 168 registers each; BN = 192: 512 threads, 128).
+template <int BN>
+struct Roles {
+    static constexpr int kEpiGroups = BN / kEpiCols;
+    static constexpr int kNumEpiWarps = 4 * kEpiGroups;
+    static constexpr int kThreads = 32 * (kEpiWarp0 + kNumEpiWarps);
+};
 constexpr int kGroupM = 16;                // m-blocks per rasterisation band
 constexpr int kMaxMaskedGroups = 1024;     // G limit of the masked layout (tile prefix in smem)
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
@@ -56,13 +67,11 @@ template <int BN, int STAGES>
 struct SmemLayout {
     static constexpr int kABytes = kBM * kBK;       // 16 KiB
     static constexpr int kBBytes = BN * kBK;
-    static constexpr int kSfaBytes = kBM * 4;
     static constexpr int kAOff = 0;
     static constexpr int kBOff = kAOff + STAGES * kABytes;
-    static constexpr int kSfaOff = kBOff + STAGES * kBBytes;
-    static constexpr int kBarOff = kSfaOff + STAGES * kSfaBytes;
-    // full[S], empty[S], tfull[4], tempty[4], drain
-    static constexpr int kNumBars = 2 * STAGES + 9;
+    static constexpr int kBarOff = kBOff + STAGES * kBBytes;
+    // full[S], empty[S], tfull[4], tempty[4], drain[2]
+    static constexpr int kNumBars = 2 * STAGES + 10;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;   // tmem base, abort flag
     static constexpr int kPrefixOff = kMiscOff + 16;
     static constexpr int kBytes = kPrefixOff + (kMaxMaskedGroups + 1) * 4;
@@ -75,6 +84,7 @@ struct Problem {
     int K;
     int G;
     int layout;
+    int ldsfa;    // row stride of SFA (round_up(M, 4))
 };
 
 struct TileInfo {
@@ -90,34 +100,40 @@ __device__ __forceinline__ void raise_status(unsigned int *status, unsigned int 
     atomicOr(status, bit);
 }
 
-// Bounded wait for the phase of `bar` with the given parity.  Gives up when
-// another role aborted or after kWaitTimeoutNs.
-__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                        unsigned int *status)
+// Slow path of wait_phase: poll until the phase completes, another role
+// aborts, or kWaitTimeoutNs passes.
+__device__ __forceinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                             unsigned int *status)
 {
-    if (mbar_try_wait(bar, parity))
-        return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity))
+    for (;;) {
+        if (mbar_test_wait(bar, parity))
             return true;
-        if ((it & 15u) == 0) {
-            if (*abort_flag)
-                return false;
-            if (global_timer_ns() - t0 > kWaitTimeoutNs) {
-                *abort_flag = 1;
-                raise_status(status, DG_DEVFLAG_TIMEOUT);
-                return false;
-            }
+        if (*abort_flag)
+            return false;
+        if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+            *abort_flag = 1;
+            raise_status(status, DG_DEVFLAG_TIMEOUT);
+            return false;
         }
     }
 }
 
+// Bounded wait for the phase of `bar` with the given parity, by one thread:
+// one inline test, then the out-of-line polling loop.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                           unsigned int *status)
+{
+    if (mbar_test_wait(bar, parity))
+        return true;
+    return wait_phase_slow(bar, parity, abort_flag, status);
+}
+
 // Bounded wait used while shutting down after an abort (ignores the flag).
-__device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
 {
     const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity))
+    while (!mbar_test_wait(bar, parity))
         if (global_timer_ns() - t0 > kWaitTimeoutNs)
             return;
 }
@@ -178,13 +194,14 @@ struct Sched {
 };
 
 template <int BN, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles<BN>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                    const __grid_constant__ CUtensorMap tmap_sfa, const float *__restrict__ sfb,
+                    const float *__restrict__ sfa, const float *__restrict__ sfb,
                     uint16_t *__restrict__ d, const int32_t *__restrict__ meta, Problem p,
                     unsigned int *status)
 {
     using L = SmemLayout<BN, STAGES>;
+    constexpr int kNumEpiWarps = Roles<BN>::kNumEpiWarps;
     // TMEM partial buffers: as many 128 x BN fp32 buffers as fit (max 4)
     constexpr int kBufs = (4 * BN <= 512) ? 4 : (512 / BN);
     constexpr uint32_t kTmemCols = (kBufs * BN <= 32)    ? 32
@@ -192,13 +209,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    : (kBufs * BN <= 128) ? 128
                                    : (kBufs * BN <= 256) ? 256
                                                          : 512;
-    constexpr int kCols = BN / kEpiGroups;             // columns per epilogue warpgroup
-    constexpr int kChunks = kCols / 32;                // 32-column TMEM loads per K block
-    constexpr uint32_t kStageTx = L::kABytes + L::kBBytes + L::kSfaBytes;
+    constexpr int kCols = kEpiCols;                    // columns per epilogue warpgroup
+    constexpr int kChunks = kCols / 16;                // 16-column TMEM loads per K block
+    constexpr uint32_t kStageTx = L::kABytes + L::kBBytes;
     constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, BN);
-    static_assert(kCols % 32 == 0 && BN <= 256, "BN must be a multiple of 64 up to 256");
-    static_assert(kCols % 128 == 0 || 128 % kCols == 0,
-                  "the columns of one epilogue warpgroup must lie in one 128-column scale block");
+    static_assert(BN % kEpiCols == 0 && BN <= 256, "BN must be a multiple of 64 up to 256");
+    static_assert(128 % kCols == 0, "the columns of one epilogue warpgroup must lie in one 128-column scale block");
     static_assert(kBufs >= 2, "at least two TMEM partial buffers");
 
     extern __shared__ uint8_t smem_raw[];
@@ -209,11 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 4 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 8);
+    auto drain_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 8 + i); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::kMiscOff + 4);
     int *prefix = reinterpret_cast<int *>(smem + L::kPrefixOff);
-    const float *sfa_smem = reinterpret_cast<const float *>(smem + L::kSfaOff);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -224,21 +239,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1 + kNumEpiWarps);
+            mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < kBufs; ++b) {
             mbar_init(tfull_bar(b), 1);
             mbar_init(tempty_bar(b), kNumEpiWarps);
         }
-        mbar_init(drain_bar, 1);
+        for (int i = 0; i < kIssuers; ++i)
+            mbar_init(drain_bar(i), 1);
         *abort_flag = 0;
         fence_mbarrier_init();
         fence_proxy_async_smem();
         tma_prefetch_desc(&tmap_a);
         tma_prefetch_desc(&tmap_b);
-        tma_prefetch_desc(&tmap_sfa);
     }
-    if (warp == 2) {
+    if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -251,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sch.prefix = prefix;
     if (p.layout == DG_LAYOUT_MASKED) {
         // per-expert tile counts from masked_m, read on the device
-        if (warp == 3) {
+        if (warp == 1) {
             const int max_mb = (p.M + kBM - 1) / kBM;
             int running = 0;
             for (int base = 0; base < p.G; base += 32) {
@@ -288,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     sch.num_tiles = (p.layout == DG_LAYOUT_MASKED) ? prefix[p.G] : sch.m_blocks * sch.n_blocks;
     const uint32_t tmem_base = *tmem_slot;
-
+    if (warp < kEpiWarp0) {
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -311,20 +326,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(fb, kStageTx);
                     const uint32_t a_dst = sbase + L::kAOff + stage * L::kABytes;
                     const uint32_t b_dst = sbase + L::kBOff + stage * L::kBBytes;
-                    const uint32_t s_dst = sbase + L::kSfaOff + stage * L::kSfaBytes;
                     const int k0 = kb * kBK;
                     if (p.layout == DG_LAYOUT_DENSE) {
                         tma_load_2d(a_dst, &tmap_a, fb, k0, ti.m0);
                         tma_load_2d(b_dst, &tmap_b, fb, k0, ti.n0);
-                        tma_load_2d(s_dst, &tmap_sfa, fb, ti.m0, kb);
                     } else if (p.layout == DG_LAYOUT_CONTIGUOUS) {
                         tma_load_2d(a_dst, &tmap_a, fb, k0, ti.m0);
                         tma_load_3d(b_dst, &tmap_b, fb, k0, ti.n0, ti.g);
-                        tma_load_2d(s_dst, &tmap_sfa, fb, ti.m0, kb);
                     } else {
                         tma_load_3d(a_dst, &tmap_a, fb, k0, ti.m0, ti.g);
                         tma_load_3d(b_dst, &tmap_b, fb, k0, ti.n0, ti.g);
-                        tma_load_3d(s_dst, &tmap_sfa, fb, ti.m0, kb, ti.g);
                     }
                     pending |= 1u << stage;
                     pending_par = (pending_par & ~(1u << stage)) | (phase << stage);
@@ -341,57 +352,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                         drain_wait(full_bar(s), (pending_par >> s) & 1u);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------ MMA issuers
+        // Two threads in two warps take alternate K blocks (by a running
+        // count over all tiles), so that one's barrier waits and commits
+        // overlap the other's MMAs.
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int buf = 0;
-            uint32_t tph = 0;
+            const uint32_t me = static_cast<uint32_t>(warp - 1);
+            const uint64_t desc_a0 = smem_desc_sw128(sbase + L::kAOff);
+            const uint64_t desc_b0 = smem_desc_sw128(sbase + L::kBOff);
+            uint32_t gkb = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < sch.num_tiles; t += gridDim.x) {
                 const TileInfo ti = sch.tile(t, p, meta);
                 if (ti.skip)
                     continue;
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = 0; kb < KB; ++kb, ++gkb) {
+                    if ((gkb % kIssuers) != me)
+                        continue;
+                    const uint32_t stage = gkb % STAGES;
+                    const uint32_t phase = (gkb / STAGES) & 1u;
+                    const uint32_t buf = gkb % kBufs;
+                    const uint32_t tph = (gkb / kBufs) & 1u;
                     if (!wait_phase(tempty_bar(buf), tph ^ 1u, abort_flag, status) ||
                         !wait_phase(full_bar(stage), phase, abort_flag, status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = sbase + L::kAOff + stage * L::kABytes;
-                    const uint32_t b_addr = sbase + L::kBOff + stage * L::kBBytes;
+                    const uint64_t da = desc_a0 + static_cast<uint64_t>((stage * L::kABytes) >> 4);
+                    const uint64_t db = desc_b0 + static_cast<uint64_t>((stage * L::kBBytes) >> 4);
                     const uint32_t d_tmem = tmem_base + buf * BN;
-#pragma unroll
-                    for (int k = 0; k < kBK / kMmaK; ++k)
-                        mma_f8f6f4(d_tmem, smem_desc_sw128(a_addr + k * kMmaK), smem_desc_sw128(b_addr + k * kMmaK),
-                                   kIdesc, k > 0 ? 1u : 0u);
+                    // 4 MMAs of K = 32 bytes; each step advances the start address by 32 B
+                    mma_f8f6f4<false>(d_tmem, da, db, kIdesc);
+                    mma_f8f6f4<true>(d_tmem, da + 2, db + 2, kIdesc);
+                    mma_f8f6f4<true>(d_tmem, da + 4, db + 4, kIdesc);
+                    mma_f8f6f4<true>(d_tmem, da + 6, db + 6, kIdesc);
                     mma_commit(empty_bar(stage));
                     mma_commit(tfull_bar(buf));
-                    if (++buf == kBufs) {
-                        buf = 0;
-                        tph ^= 1u;
-                    }
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
                 }
             }
-            // every MMA issued above has completed once this barrier flips
-            mma_commit(drain_bar);
-            drain_wait(drain_bar, 0);
+            // every MMA this thread issued has completed once this barrier flips
+            mma_commit(drain_bar(me));
+            drain_wait(drain_bar(me), 0);
         }
-    } else if (warp >= kEpiWarp0) {
+    }
+    } else {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;                          // TMEM lane quarter of this warp
-        const int grp = (warp - kEpiWarp0) >> 2;         // column half of this warpgroup
+        const int grp = (warp - kEpiWarp0) >> 2;         // column slice of this warpgroup
         const int r = q * 32 + lane;                     // row of the tile owned by this thread
         const int c0 = grp * kCols;                      // first column of this warpgroup
         const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c0;
-        int stage = 0;
-        uint32_t phase = 0;
         int buf = 0;
         uint32_t tph = 0;
         bool ok = true;
@@ -418,10 +430,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            // this row's activation scales: sfa[kb][m] (masked: per expert),
+            // read ahead four K blocks; rows outside A read nothing
+            const bool row_in = ti.m0 + r < p.M;
+            const float *sfa_row = sfa + (p.layout == DG_LAYOUT_MASKED ? static_cast<size_t>(ti.g) * KB * p.ldsfa : 0) +
+                                   ti.m0 + r;
+            auto load_sa = [&](int kb) -> float {
+                return (row_in && kb < KB) ? __ldg(sfa_row + static_cast<size_t>(kb) * p.ldsfa) : 0.0f;
+            };
+            float sa0 = load_sa(0), sa1 = load_sa(1), sa2 = load_sa(2), sa3 = load_sa(3);
             // the 128-column scale block of B holding this warpgroup's columns
             const int nb = min((ti.n0 + c0) >> 7, NBs - 1);
             const float *sfb_row = sfb + (static_cast<size_t>(ti.g) * NBs + nb) * KB;
-            float sb_next = __ldg(sfb_row);
+            float sb0 = __ldg(sfb_row), sb1 = KB > 1 ? __ldg(sfb_row + 1) : 0.0f;
 
             float2 acc[kCols / 2];
 #pragma unroll
@@ -429,38 +450,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc[j] = make_float2(0.0f, 0.0f);
 
             for (int kb = 0; kb < KB; ++kb) {
-                const bool got = wait_phase(tfull_bar(buf), tph, abort_flag, status) &&
-                                 wait_phase(full_bar(stage), phase, abort_flag, status);
-                if (!__all_sync(0xffffffffu, got)) {
+                // fp32 product of the two scales, rounded once
+                const float s = sa0 * sb0;
+                const float2 s2 = make_float2(s, s);
+                sa0 = sa1;
+                sa1 = sa2;
+                sa2 = sa3;
+                sa3 = load_sa(kb + 4);
+                sb0 = sb1;
+                sb1 = kb + 2 < KB ? __ldg(sfb_row + kb + 2) : 0.0f;
+                // wait until the MMAs of this K block are complete: one thread
+                // polls the barrier, the named barrier releases the other
+                // epilogue threads and shares the outcome
+                bool got = true;
+                if (threadIdx.x == kEpiWarp0 * 32)
+                    got = wait_phase(tfull_bar(buf), tph, abort_flag, status);
+                if (!named_barrier_and(1, kNumEpiWarps * 32, got)) {
                     ok = false;
                     break;
                 }
-                // fp32 product of the two scales, rounded once
-                const float s = sfa_smem[stage * kBM + r] * sb_next;
-                const float2 s2 = make_float2(s, s);
-                if (kb + 1 < KB)
-                    sb_next = __ldg(sfb_row + kb + 1);
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(empty_bar(stage));
                 tc_fence_after();
                 const uint32_t t_buf = t_lane + buf * BN;
-                uint32_t v0[32], v1[32];
-                tmem_ld32(t_buf, v0);
-                tmem_wait_ld32(v0);
+                uint32_t v0[16], v1[16];
+                tmem_ld16(t_buf, v0);
+                tmem_wait_ld16(v0);
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c) {
-                    uint32_t(&cur)[32] = (c & 1) ? v1 : v0;
-                    uint32_t(&nxt)[32] = (c & 1) ? v0 : v1;
+                    uint32_t(&cur)[16] = (c & 1) ? v1 : v0;
+                    uint32_t(&nxt)[16] = (c & 1) ? v0 : v1;
                     if (c + 1 < kChunks)
-                        tmem_ld32(t_buf + (c + 1) * 32, nxt);
+                        tmem_ld16(t_buf + (c + 1) * 16, nxt);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        acc[c * 16 + j] =
+                    for (int j = 0; j < 8; ++j)
+                        acc[c * 8 + j] =
                             ffma2(make_float2(__uint_as_float(cur[2 * j]), __uint_as_float(cur[2 * j + 1])), s2,
-                                  acc[c * 16 + j]);
+                                  acc[c * 8 + j]);
                     if (c + 1 < kChunks)
-                        tmem_wait_ld32(nxt);
+                        tmem_wait_ld16(nxt);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -469,10 +495,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (++buf == kBufs) {
                     buf = 0;
                     tph ^= 1u;
-                }
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
                 }
             }
             if (!ok)
@@ -494,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 2) {
+    if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
     }
@@ -509,24 +531,36 @@ struct Plan {
     int smem;
 };
 
-constexpr int kBN = 128;
-constexpr int kStages = 6;
+// Tile configurations compiled in: 128 x 192 with 5 stages (two TMEM partial
+// buffers) for problems with at least one full wave of such tiles, 128 x 128
+// with 6 stages (four buffers) otherwise.
+constexpr int kStages192 = 5;
+constexpr int kStages128 = 6;
+
+int forced_bn()
+{
+    // DG_FORCE_BN=128|192 pins the tile width (tests and sweeps)
+    const char *e = getenv("DG_FORCE_BN");
+    const int b = e ? atoi(e) : 0;
+    return (b == 128 || b == 192) ? b : 0;
+}
 
 Plan make_plan(int layout, int M, int N, int K, int G, int num_sms)
 {
     (void)K;
     Plan pl;
-    pl.bn = kBN;
-    pl.stages = kStages;
-    pl.smem = SmemLayout<kBN, kStages>::kAlloc;
-    const int nblk = ceil_div(N, pl.bn);
-    if (layout == DG_LAYOUT_MASKED) {
-        pl.num_tiles = G * ceil_div(M, kBM) * nblk;
+    const int mblk = layout == DG_LAYOUT_MASKED ? G * ceil_div(M, kBM) : ceil_div(M, kBM);
+    int bn = forced_bn();
+    if (bn == 0)
+        bn = (mblk * ceil_div(N, 192) >= num_sms) ? 192 : 128;
+    pl.bn = bn;
+    pl.stages = bn == 192 ? kStages192 : kStages128;
+    pl.smem = bn == 192 ? SmemLayout<192, kStages192>::kAlloc : SmemLayout<128, kStages128>::kAlloc;
+    pl.num_tiles = mblk * ceil_div(N, bn);
+    if (layout == DG_LAYOUT_MASKED)
         pl.grid = num_sms;   // fixed: the real tile count is only known on the device
-    } else {
-        pl.num_tiles = ceil_div(M, kBM) * nblk;
+    else
         pl.grid = pl.num_tiles < num_sms ? pl.num_tiles : num_sms;
-    }
     if (pl.grid < 1)
         pl.grid = 1;
     return pl;
@@ -552,10 +586,9 @@ dg_status_t launch(int layout, const uint8_t *a, const float *sfa, const uint8_t
     if (st != DG_OK)
         return st;
     const Plan pl = make_plan(layout, M, N, K, G, info.sm_count);
-    const int KB = K / kBK;
     const int ldsfa = round_up(M, 4);
 
-    CUtensorMap ta, tb, ts;
+    CUtensorMap ta, tb;
     {
         // A: E4M3 [rows][K] (dense / contiguous) or [G][max_m][K] (masked)
         const uint64_t dims3[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint64_t>(G)};
@@ -577,24 +610,15 @@ dg_status_t launch(int layout, const uint8_t *a, const float *sfa, const uint8_t
         if (st != DG_OK)
             return st;
     }
-    {
-        // SFA: fp32 [K/128][ldsfa] (dense / contiguous) or [G][K/128][ldsfa]
-        const uint64_t dims3[3] = {static_cast<uint64_t>(M), static_cast<uint64_t>(KB), static_cast<uint64_t>(G)};
-        const uint64_t strides[2] = {static_cast<uint64_t>(ldsfa) * 4, static_cast<uint64_t>(ldsfa) * 4 * KB};
-        const uint32_t box[3] = {kBM, 1, 1};
-        st = encode_tensor_map(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, layout == DG_LAYOUT_MASKED ? 3 : 2, sfa, dims3,
-                               strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
-        if (st != DG_OK)
-            return st;
-    }
-    auto kernel = fp8_gemm_kernel<kBN, kStages>;
+    auto kernel = pl.bn == 192 ? fp8_gemm_kernel<192, kStages192> : fp8_gemm_kernel<128, kStages128>;
+    const int threads = pl.bn == 192 ? Roles<192>::kThreads : Roles<128>::kThreads;
     st = ensure_smem_attr(reinterpret_cast<const void *>(kernel), pl.smem);
     if (st != DG_OK)
         return st;
-    Problem prob{M, N, K, G, layout};
+    Problem prob{M, N, K, G, layout, ldsfa};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pl.grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
@@ -602,7 +626,7 @@ dg_status_t launch(int layout, const uint8_t *a, const float *sfa, const uint8_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, ts, sfb, d, meta, prob, info.status_word) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, sfa, sfb, d, meta, prob, info.status_word) != cudaSuccess)
         return DG_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }

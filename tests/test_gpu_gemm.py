@@ -21,6 +21,14 @@ def built():
     dg.dg_read_device_status()
 
 
+@pytest.fixture(params=[128, 192], ids=["bn128", "bn192"])
+def tile_n(request, monkeypatch):
+    """Runs the test with each compiled tile width (the plan's choice is
+    pinned through DG_FORCE_BN)."""
+    monkeypatch.setenv("DG_FORCE_BN", str(request.param))
+    return request.param
+
+
 def dev(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
@@ -38,17 +46,17 @@ def gpu_dense(a, sfa, b, sfb):
 
 # ------------------------------------------------------------------ dense --
 DENSE_SHAPES = [(128, 256, 512), (1, 128, 128), (129, 136, 384), (300, 392, 640), (513, 1024, 256),
-                (256, 2112, 1024)]
+                (256, 2112, 1024), (1100, 1288, 384), (4224, 1288, 256)]
 
 
 @pytest.mark.parametrize("M,N,K", DENSE_SHAPES)
-def test_dense_exact_bit_identical(M, N, K):
+def test_dense_exact_bit_identical(M, N, K, tile_n):
     a, sfa, b, sfb = exact_dense(M, N, K, seed=M * 3 + N + K)
     np.testing.assert_array_equal(gpu_dense(a, sfa, b, sfb), oracle.gemm_nt(a, sfa, b, sfb))
 
 
 @pytest.mark.parametrize("M,N,K", DENSE_SHAPES)
-def test_dense_random_tolerance(M, N, K):
+def test_dense_random_tolerance(M, N, K, tile_n):
     a, sfa, b, sfb = random_dense(M, N, K, seed=M + 5 * N + K, outliers=True)
     ref = oracle.gemm_nt(a, sfa, b, sfb)
     tolerance_check(bf16_bits_to_f32(gpu_dense(a, sfa, b, sfb)), bf16_bits_to_f32(ref), f"dense {M}x{N}x{K}")
@@ -110,7 +118,7 @@ def gpu_contiguous(a, sfa, b, sfb, m_indices):
 
 
 @pytest.mark.parametrize("G,tokens,N,K", [(4, 700, 256, 512), (8, 1500, 392, 384), (3, 129, 128, 128)])
-def test_contiguous_exact_bit_identical(G, tokens, N, K):
+def test_contiguous_exact_bit_identical(G, tokens, N, K, tile_n):
     a, sfa, b, sfb, mi = contiguous_case(G, tokens, N, K, seed=G + tokens, exact=True)
     ref = np.full((a.shape[0], N), wl.SENTINEL_BF16, dtype=np.uint16)
     ref = oracle.grouped_contiguous(a, sfa, b, sfb, mi, d=ref)
@@ -118,7 +126,7 @@ def test_contiguous_exact_bit_identical(G, tokens, N, K):
 
 
 @pytest.mark.parametrize("G,tokens,N,K", [(8, 2000, 512, 1024), (2, 300, 264, 256)])
-def test_contiguous_random_tolerance(G, tokens, N, K):
+def test_contiguous_random_tolerance(G, tokens, N, K, tile_n):
     a, sfa, b, sfb, mi = contiguous_case(G, tokens, N, K, seed=7 * G + tokens, exact=False)
     out = gpu_contiguous(a, sfa, b, sfb, mi)
     ref = oracle.grouped_contiguous(a, sfa, b, sfb, mi)
@@ -174,14 +182,14 @@ def gpu_masked(a, sfa, b, sfb, masked_m):
     (3, 200, 392, 384, [200, 129, 128]),
     (2, 64, 128, 128, [64, 3]),
 ])
-def test_masked_exact_bit_identical(G, max_m, N, K, mm):
+def test_masked_exact_bit_identical(G, max_m, N, K, mm, tile_n):
     a, sfa, b, sfb, masked_m = masked_case(G, max_m, N, K, mm, seed=G * 11 + max_m, exact=True)
     ref = oracle.grouped_masked(a, sfa, b, sfb, masked_m,
                                 d=np.full((G, max_m, N), wl.SENTINEL_BF16, np.uint16))
     np.testing.assert_array_equal(gpu_masked(a, sfa, b, sfb, masked_m), ref)
 
 
-def test_masked_random_tolerance():
+def test_masked_random_tolerance(tile_n):
     G, max_m, N, K = 6, 256, 512, 1024
     mm = wl.masked_counts(G, max_m, seed=12)
     a, sfa, b, sfb, masked_m = masked_case(G, max_m, N, K, mm, seed=12, exact=False)
@@ -204,7 +212,7 @@ def test_masked_clamps_and_flags_bad_counts():
     np.testing.assert_array_equal(out, ref)
 
 
-def test_masked_cuda_graph_replay_follows_device_counts():
+def test_masked_cuda_graph_replay_follows_device_counts(tile_n):
     G, max_m, N, K = 4, 256, 256, 512
     a, sfa, b, sfb, _ = masked_case(G, max_m, N, K, [0] * G, seed=31, exact=True)
     ta, tsa, tb, tsb = dev(a), dev(sfa), dev(b), dev(sfb)
