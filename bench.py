@@ -152,6 +152,25 @@ def algorithmic_bytes(w: wl.Workload):
     return useful * K + experts * N * K + useful * KB * 4 + experts * NB * KB * 4 + useful * N * 2
 
 
+# ------------------------------------------------------------- replicas ----
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest value over all ranks (the job's time is its slowest
+    replica's); a no-op without an initialised process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, units_per_rank_step: float, steps: int, max_ms: float) -> float:
+    """Whole-job rate: every replica processes its own units; the job takes
+    the slowest replica's time (weak scaling, no data-path collective)."""
+    return world * units_per_rank_step * steps / (max_ms * 1e-3)
+
+
 # ---------------------------------------------------------------- CPU leg --
 def cpu_oracle_rate(w: wl.Workload, seconds: float):
     """Time the oracle (quantise + GEMM) over whole rows of the workload,
@@ -322,10 +341,7 @@ def run_gpu(args, w):
     # per-kernel durations: the same launches, one kernel kind per graph
     gemm_ms = timed(g_gemm, reps)
     quant_ms = timed(g_quant, reps)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, device=dev)
 
     # end to end: pinned host activations in, bf16 result out, every step
     x_pin = torch.from_numpy(x_host).pin_memory()
@@ -349,8 +365,9 @@ def run_gpu(args, w):
     e2e_ms = e0.elapsed_time(e1)
 
     flops_step = 2.0 * M * N * K
-    value = world * flops_step * steps_run / (total_ms * 1e-3) / 1e12
-    e2e_value = world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    value = job_throughput(world, flops_step, steps_run, total_ms) / 1e12
+    e2e_ms = max_over_ranks(e2e_ms, device=dev)
+    e2e_value = job_throughput(world, flops_step, e2e_steps, e2e_ms) / 1e12
 
     hbm, bf16, bf16_sus, src = peaks()
     fp8_peak = bf16 * FP8_PER_BF16

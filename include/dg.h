@@ -141,8 +141,9 @@ dg_status_t dg_fp8_grouped_masked(const uint8_t *a, const float *sfa, const uint
  * problem on a GPU with `num_sms` SMs (num_sms <= 0: the current device's).
  * Makes no CUDA call when num_sms > 0.  For DG_LAYOUT_DENSE, M is the row
  * count; CONTIGUOUS: M = sum_M; MASKED: M = max_m.  Tiles are 128 x 192 when
- * the problem has at least one full wave of them, else 128 x 128; the
- * environment variable DG_FORCE_BN=128|192 (read at every call) pins the
+ * the problem has at least one full wave of them; otherwise 128 x 128 or
+ * 128 x 96, whichever leaves the busiest CTA the fewest operand bytes; the
+ * environment variable DG_FORCE_BN=96|128|192 (read at every call) pins the
  * width.  Results do not depend on the tile width. */
 dg_status_t dg_query_plan(int layout, int M, int N, int K, int G, int num_sms, dg_plan_t *out);
 

@@ -30,11 +30,14 @@
 //               bf16 and stores the row.
 // Tiles are 128 x 192 (two TMEM buffers, three epilogue warpgroups, 512
 // threads) when the problem has at least a full wave of them, else 128 x 128
-// (four buffers, two epilogue warpgroups, 384 threads).
+// (four buffers, two warpgroups, 384 threads) or 128 x 96 (four buffers,
+// three 32-column warpgroups), whichever fills the SMs better.  The output
+// tile is staged per warp in shared memory and stored row-major, so that
+// each store instruction writes whole row segments.
 // Tiles are visited in a grouped order (GROUP_M m-blocks per band) so that the
 // CTAs running at the same time share A and B tiles through L2.
 //
-// Every wait is bounded: after kWaitTimeoutNs a role raises the CTA's abort
+// Every wait is bounded: after kWaitTimeoutCycles a role raises the CTA's abort
 // flag and DG_DEVFLAG_TIMEOUT, the producer waits (bounded) for its own copies
 // in flight, the MMA thread drains its MMAs, TMEM is freed and the CTA exits.
 #include <stdlib.h>
@@ -48,28 +51,35 @@ namespace {
 constexpr int kBM = 128;                   // rows per tile (tcgen05 M)
 constexpr int kBK = 128;                   // K per stage = one promotion block = one 128-byte row
 constexpr int kEpiWarp0 = 4;                        // warps 0-3: producer, two MMA issuers, spare
-constexpr int kEpiCols = 64;                        // tile columns per epilogue warpgroup
 constexpr int kIssuers = 2;                         // MMA-issuing threads (warps 1 and 2)
 
-// Threads of the CTA for a tile width: 4 warps + one warpgroup per 64 columns
-// (BN = 128: 384 threads, 168 registers each; BN = 192: 512 threads, 128).
-template <int BN>
+// Threads of the CTA for a tile width: 4 warps + one epilogue warpgroup per
+// EPI_COLS columns (BN = 96: 3 x 32 columns, 512 threads; BN = 128: 2 x 64,
+// 384 threads, 168 registers each; BN = 192: 3 x 64, 512 threads, 128).
+template <int BN, int EPI_COLS>
 struct Roles {
-    static constexpr int kEpiGroups = BN / kEpiCols;
+    static constexpr int kEpiGroups = BN / EPI_COLS;
     static constexpr int kNumEpiWarps = 4 * kEpiGroups;
     static constexpr int kThreads = 32 * (kEpiWarp0 + kNumEpiWarps);
 };
 constexpr int kGroupM = 16;                // m-blocks per rasterisation band
 constexpr int kMaxMaskedGroups = 1024;     // G limit of the masked layout (tile prefix in smem)
-constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+// Pipeline waits give up after this many SM cycles (about 2 s at 2 GHz).
+constexpr long long kWaitTimeoutCycles = 4000000000ll;
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int EPI_COLS>
 struct SmemLayout {
     static constexpr int kABytes = kBM * kBK;       // 16 KiB
     static constexpr int kBBytes = BN * kBK;
     static constexpr int kAOff = 0;
     static constexpr int kBOff = kAOff + STAGES * kABytes;
-    static constexpr int kBarOff = kBOff + STAGES * kBBytes;
+    // output staging: each epilogue warp owns 32 rows x EPI_COLS bf16, rows
+    // padded by 16 bytes so that row-per-thread 16-byte writes do not collide
+    // on shared-memory banks
+    static constexpr int kOutRowStride = EPI_COLS * 2 + 16;
+    static constexpr int kOutWarpBytes = 32 * kOutRowStride;
+    static constexpr int kOutOff = kBOff + STAGES * kBBytes;
+    static constexpr int kBarOff = kOutOff + (BN / EPI_COLS) * 4 * kOutWarpBytes;
     // full[S], empty[S], tfull[4], tempty[4], drain[2]
     static constexpr int kNumBars = 2 * STAGES + 10;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;   // tmem base, abort flag
@@ -101,20 +111,24 @@ __device__ __forceinline__ void raise_status(unsigned int *status, unsigned int 
 }
 
 // Slow path of wait_phase: poll until the phase completes, another role
-// aborts, or kWaitTimeoutNs passes.
+// aborts, or about kWaitTimeoutCycles SM cycles pass.  The clock and the
+// abort flag are looked at every 64 polls only: a timer read is far slower
+// than a barrier test (%globaltimer costs hundreds of cycles).
 __device__ __forceinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                             unsigned int *status)
+                                                unsigned int *status)
 {
-    const uint64_t t0 = global_timer_ns();
-    for (;;) {
+    const long long t0 = clock64();
+    for (uint32_t it = 1;; ++it) {
         if (mbar_test_wait(bar, parity))
             return true;
-        if (*abort_flag)
-            return false;
-        if (global_timer_ns() - t0 > kWaitTimeoutNs) {
-            *abort_flag = 1;
-            raise_status(status, DG_DEVFLAG_TIMEOUT);
-            return false;
+        if ((it & 63u) == 0) {
+            if (*abort_flag)
+                return false;
+            if (clock64() - t0 > kWaitTimeoutCycles) {
+                *abort_flag = 1;
+                raise_status(status, DG_DEVFLAG_TIMEOUT);
+                return false;
+            }
         }
     }
 }
@@ -132,9 +146,9 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 // Bounded wait used while shutting down after an abort (ignores the flag).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
 {
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_test_wait(bar, parity))
-        if (global_timer_ns() - t0 > kWaitTimeoutNs)
+    const long long t0 = clock64();
+    for (uint32_t it = 1; !mbar_test_wait(bar, parity); ++it)
+        if ((it & 63u) == 0 && clock64() - t0 > kWaitTimeoutCycles)
             return;
 }
 
@@ -193,15 +207,15 @@ struct Sched {
     }
 };
 
-template <int BN, int STAGES>
-__global__ void __launch_bounds__(Roles<BN>::kThreads, 1)
+template <int BN, int STAGES, int EPI_COLS>
+__global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const float *__restrict__ sfa, const float *__restrict__ sfb,
                     uint16_t *__restrict__ d, const int32_t *__restrict__ meta, Problem p,
                     unsigned int *status)
 {
-    using L = SmemLayout<BN, STAGES>;
-    constexpr int kNumEpiWarps = Roles<BN>::kNumEpiWarps;
+    using L = SmemLayout<BN, STAGES, EPI_COLS>;
+    constexpr int kNumEpiWarps = Roles<BN, EPI_COLS>::kNumEpiWarps;
     // TMEM partial buffers: as many 128 x BN fp32 buffers as fit (max 4)
     constexpr int kBufs = (4 * BN <= 512) ? 4 : (512 / BN);
     constexpr uint32_t kTmemCols = (kBufs * BN <= 32)    ? 32
@@ -209,11 +223,11 @@ __global__ void __launch_bounds__(Roles<BN>::kThreads, 1)
                                    : (kBufs * BN <= 128) ? 128
                                    : (kBufs * BN <= 256) ? 256
                                                          : 512;
-    constexpr int kCols = kEpiCols;                    // columns per epilogue warpgroup
+    constexpr int kCols = EPI_COLS;                    // columns per epilogue warpgroup
     constexpr int kChunks = kCols / 16;                // 16-column TMEM loads per K block
     constexpr uint32_t kStageTx = L::kABytes + L::kBBytes;
     constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, BN);
-    static_assert(BN % kEpiCols == 0 && BN <= 256, "BN must be a multiple of 64 up to 256");
+    static_assert(BN % EPI_COLS == 0 && EPI_COLS % 16 == 0 && BN <= 256, "BN must be a multiple of EPI_COLS up to 256");
     static_assert(128 % kCols == 0, "the columns of one epilogue warpgroup must lie in one 128-column scale block");
     static_assert(kBufs >= 2, "at least two TMEM partial buffers");
 
@@ -499,16 +513,35 @@ __global__ void __launch_bounds__(Roles<BN>::kThreads, 1)
             }
             if (!ok)
                 break;
-            if (row_ok) {
-                uint16_t *dst = d + d_row * p.N + ti.n0 + c0;
+            // Store: each thread writes its row into the warp's staging rows,
+            // then the warp writes 32 rows x kCols out row-major, so that one
+            // instruction covers whole row segments.  Rows that must not be
+            // written (edges, masked tails, padding) are skipped.
+            {
+                uint8_t *const stage = smem + L::kOutOff + (warp - kEpiWarp0) * L::kOutWarpBytes;
+                const uint32_t my_row = smem_u32(stage) + lane * L::kOutRowStride;
 #pragma unroll
-                for (int c = 0; c < kCols / 8; ++c) {
-                    if (ti.n0 + c0 + c * 8 < p.N)
-                        st_global_v4(dst + c * 8, pack_bf16x2(acc[c * 4 + 0].x, acc[c * 4 + 0].y),
-                                     pack_bf16x2(acc[c * 4 + 1].x, acc[c * 4 + 1].y),
-                                     pack_bf16x2(acc[c * 4 + 2].x, acc[c * 4 + 2].y),
-                                     pack_bf16x2(acc[c * 4 + 3].x, acc[c * 4 + 3].y));
+                for (int c = 0; c < kCols / 8; ++c)
+                    st_shared_v4(my_row + c * 16, pack_bf16x2(acc[c * 4 + 0].x, acc[c * 4 + 0].y),
+                                 pack_bf16x2(acc[c * 4 + 1].x, acc[c * 4 + 1].y),
+                                 pack_bf16x2(acc[c * 4 + 2].x, acc[c * 4 + 2].y),
+                                 pack_bf16x2(acc[c * 4 + 3].x, acc[c * 4 + 3].y));
+                __syncwarp();
+                const uint32_t rows_ok = __ballot_sync(0xffffffffu, row_ok);
+                const size_t warp_row0 = d_row - lane;           // D row of this warp's first row
+                constexpr int kChunksPerRow = kCols / 8;         // 16-byte chunks per staged row
+#pragma unroll
+                for (int i = 0; i < kChunksPerRow; ++i) {
+                    const int idx = i * 32 + lane;
+                    const int rr = idx / kChunksPerRow;
+                    const int cc = idx % kChunksPerRow;
+                    const int col = ti.n0 + c0 + cc * 8;
+                    if (((rows_ok >> rr) & 1u) && col < p.N) {
+                        const uint4 v = ld_shared_v4(smem_u32(stage) + rr * L::kOutRowStride + cc * 16);
+                        st_global_v4(d + (warp_row0 + rr) * p.N + col, v.x, v.y, v.z, v.w);
+                    }
                 }
+                __syncwarp();
             }
         }
     }
@@ -531,18 +564,35 @@ struct Plan {
     int smem;
 };
 
-// Tile configurations compiled in: 128 x 192 with 5 stages (two TMEM partial
-// buffers) for problems with at least one full wave of such tiles, 128 x 128
-// with 6 stages (four buffers) otherwise.
-constexpr int kStages192 = 5;
-constexpr int kStages128 = 6;
+// Tile configurations compiled in (width, stages, epilogue columns per
+// warpgroup).  The plan takes 128 x 192 when the problem has at least one full
+// wave of such tiles; otherwise the narrower width whose busiest CTA streams
+// the fewest bytes: waves x (128 + BN) rows of operand per K block.  For
+// M = 256, N = 7168 on 152 SMs that is BN = 96 (150 tiles, one wave) over
+// BN = 128 (112 tiles), the pages' 112-versus-128 argument redone for this
+// SM count.
+struct TileCfg {
+    int bn;
+    int stages;
+    int epi_cols;
+};
+constexpr TileCfg kCfg96{96, 6, 32};
+constexpr TileCfg kCfg128{128, 5, 64};
+constexpr TileCfg kCfg192{192, 4, 64};
 
 int forced_bn()
 {
-    // DG_FORCE_BN=128|192 pins the tile width (tests and sweeps)
+    // DG_FORCE_BN=96|128|192 pins the tile width (tests and sweeps)
     const char *e = getenv("DG_FORCE_BN");
     const int b = e ? atoi(e) : 0;
-    return (b == 128 || b == 192) ? b : 0;
+    return (b == 96 || b == 128 || b == 192) ? b : 0;
+}
+
+int smem_for(int bn)
+{
+    return bn == 192 ? SmemLayout<192, kCfg192.stages, kCfg192.epi_cols>::kAlloc
+           : bn == 96 ? SmemLayout<96, kCfg96.stages, kCfg96.epi_cols>::kAlloc
+                      : SmemLayout<128, kCfg128.stages, kCfg128.epi_cols>::kAlloc;
 }
 
 Plan make_plan(int layout, int M, int N, int K, int G, int num_sms)
@@ -551,11 +601,25 @@ Plan make_plan(int layout, int M, int N, int K, int G, int num_sms)
     Plan pl;
     const int mblk = layout == DG_LAYOUT_MASKED ? G * ceil_div(M, kBM) : ceil_div(M, kBM);
     int bn = forced_bn();
-    if (bn == 0)
-        bn = (mblk * ceil_div(N, 192) >= num_sms) ? 192 : 128;
+    if (bn == 0) {
+        if (static_cast<long long>(mblk) * ceil_div(N, 192) >= num_sms) {
+            bn = 192;
+        } else {
+            long long best = -1;
+            for (int cand : {128, 96}) {
+                const long long tiles = static_cast<long long>(mblk) * ceil_div(N, cand);
+                const long long waves = (tiles + num_sms - 1) / num_sms;
+                const long long cost = waves * (kBM + cand);
+                if (best < 0 || cost < best) {
+                    best = cost;
+                    bn = cand;
+                }
+            }
+        }
+    }
     pl.bn = bn;
-    pl.stages = bn == 192 ? kStages192 : kStages128;
-    pl.smem = bn == 192 ? SmemLayout<192, kStages192>::kAlloc : SmemLayout<128, kStages128>::kAlloc;
+    pl.stages = bn == 192 ? kCfg192.stages : bn == 96 ? kCfg96.stages : kCfg128.stages;
+    pl.smem = smem_for(bn);
     pl.num_tiles = mblk * ceil_div(N, bn);
     if (layout == DG_LAYOUT_MASKED)
         pl.grid = num_sms;   // fixed: the real tile count is only known on the device
@@ -610,8 +674,12 @@ dg_status_t launch(int layout, const uint8_t *a, const float *sfa, const uint8_t
         if (st != DG_OK)
             return st;
     }
-    auto kernel = pl.bn == 192 ? fp8_gemm_kernel<192, kStages192> : fp8_gemm_kernel<128, kStages128>;
-    const int threads = pl.bn == 192 ? Roles<192>::kThreads : Roles<128>::kThreads;
+    auto kernel = pl.bn == 192  ? fp8_gemm_kernel<192, kCfg192.stages, kCfg192.epi_cols>
+                  : pl.bn == 96 ? fp8_gemm_kernel<96, kCfg96.stages, kCfg96.epi_cols>
+                                : fp8_gemm_kernel<128, kCfg128.stages, kCfg128.epi_cols>;
+    const int threads = pl.bn == 192  ? Roles<192, kCfg192.epi_cols>::kThreads
+                        : pl.bn == 96 ? Roles<96, kCfg96.epi_cols>::kThreads
+                                      : Roles<128, kCfg128.epi_cols>::kThreads;
     st = ensure_smem_attr(reinterpret_cast<const void *>(kernel), pl.smem);
     if (st != DG_OK)
         return st;

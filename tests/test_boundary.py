@@ -84,14 +84,25 @@ def test_read_status_validation(lib):
 
 
 def test_plan_tile_arithmetic_of_the_pages():
-    # M=256, N=7168: 128-wide blocks give 2 x 56 = 112 tiles (the page's
-    # "112 compute units"); the 112-wide alternative would give 2 x 64 = 128.
+    # M=256, N=7168 ("DeepGEMM：一款支持FP8通用矩阵乘法(GEMM)的开源库", 非标准块大小支持):
+    # 128-wide blocks give 2 x 56 = 112 tiles, 112-wide ones 2 x 64 = 128.
+    assert 2 * (7168 // 128) == 112 and 2 * (7168 // 112) == 128
+    # With 132 SMs the plan keeps 128-wide tiles (112 tiles, one wave) ...
     p = dg.dg_query_plan(dg.DG_LAYOUT_DENSE, 256, 7168, 2048, 1, num_sms=132)
-    assert p["block_m"] == 128
-    assert p["num_tiles"] == (256 // p["block_m"]) * (-(-7168 // p["block_n"]))
-    if p["block_n"] == 128:
-        assert p["num_tiles"] == 112
-    assert 2 * (7168 // 112) == 128
+    assert (p["block_m"], p["block_n"], p["num_tiles"], p["grid"]) == (128, 128, 112, 112)
+    # ... and with 152 SMs it narrows them to 96 so that 150 of 152 SMs work.
+    p = dg.dg_query_plan(dg.DG_LAYOUT_DENSE, 256, 7168, 2048, 1, num_sms=152)
+    assert (p["block_n"], p["num_tiles"], p["grid"]) == (96, 150, 150)
+
+
+def test_plan_width_override(monkeypatch):
+    for bn in (96, 128, 192):
+        monkeypatch.setenv("DG_FORCE_BN", str(bn))
+        p = dg.dg_query_plan(dg.DG_LAYOUT_DENSE, 4096, 7168, 2048, 1, num_sms=152)
+        assert p["block_n"] == bn and p["num_tiles"] == 32 * -(-7168 // bn)
+    monkeypatch.setenv("DG_FORCE_BN", "100")   # not a compiled width: ignored
+    p = dg.dg_query_plan(dg.DG_LAYOUT_DENSE, 4096, 7168, 2048, 1, num_sms=152)
+    assert p["block_n"] == 192
 
 
 def test_plan_shapes():

@@ -1,0 +1,115 @@
+"""Parity at the full sizes of the five workloads, in the launch configuration
+the benchmark uses (the plan the library picks, programmatic dependent launch),
+on sampled output rows the oracle computes one by one.  Inputs are the seeded
+fp32 workloads quantised by the oracle; the GPU quantiser is checked against
+the oracle on the same activations."""
+import numpy as np
+import pytest
+import torch
+
+import moe_grouped_gemm_x128_gb300 as dg
+import oracle
+import workloads as wl
+from helpers import QB, bf16_bits_to_f32, tolerance_check
+
+pytestmark = pytest.mark.gpu
+
+N_SAMPLE = 48
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    dg.build()
+    dg.load()
+    dg.dg_read_device_status()
+    yield
+    assert not (dg.dg_read_device_status() & dg.DG_DEVFLAG_TIMEOUT)
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def bits(t):
+    torch.cuda.synchronize()
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def edge_rows(M):
+    return [0, 1, 127, 128, M - 1, M - 2]
+
+
+@pytest.mark.parametrize("name", ["skinny", "sweep_n7168_k18432", "sweep_n24576_k1536", "sweep_n2112_k7168"])
+def test_dense_full_size_sampled(name):
+    w = wl.WORKLOADS[name]
+    x, wt = wl.dense_inputs(w.M, w.N, w.K, w.seed, w.outliers)
+    a, sfa = oracle.quant_act_1x128(x)
+    b, sfb = oracle.quant_weight_128x128(wt)
+    # the GPU quantiser agrees with the oracle on the whole activation matrix
+    qa, sa = dg.dg_quant_act_1x128(dev(x))
+    np.testing.assert_array_equal(qa.cpu().numpy(), a)
+    np.testing.assert_array_equal(sa.cpu().numpy()[:, :w.M], sfa[:, :w.M])
+    d = dg.dg_fp8_gemm_nt(qa, sa, dev(b), dev(sfb))
+    out = bits(d)
+    rows = wl.sample_rows(w.M, N_SAMPLE, w.seed, must=edge_rows(w.M))
+    ref = oracle.gemm_nt(a, sfa, b, sfb, rows=rows)
+    tolerance_check(bf16_bits_to_f32(out[rows]), bf16_bits_to_f32(ref[rows]), name)
+
+
+def test_contiguous_full_size_sampled():
+    w = wl.WORKLOADS["contig"]
+    x, wt, m_indices, counts = wl.contiguous_inputs(w)
+    a, sfa = oracle.quant_act_1x128(x)
+    b, sfb = oracle.quant_weight_128x128(wt)
+    sent = wl.SENTINEL_BF16
+    d = torch.full((len(m_indices), w.N), sent, dtype=torch.int16, device="cuda")
+    dg.dg_fp8_grouped_contiguous(dev(a), dev(sfa), dev(b), dev(sfb), dev(m_indices), d.view(torch.bfloat16))
+    out = bits(d.view(torch.bfloat16))
+    # rows of every expert (its first and last rows) plus a random sample
+    _, _, seg = wl.contiguous_routing(w.G, w.tokens, w.seed)
+    must = []
+    for e in range(w.G):
+        must += [int(seg[e]), int(seg[e] + counts[e] - 1)]
+    rows = wl.sample_rows(len(m_indices), N_SAMPLE, w.seed, must=must)
+    ref = oracle.grouped_contiguous(a, sfa, b, sfb, m_indices, rows=rows,
+                                    d=np.full((len(m_indices), w.N), sent, np.uint16))
+    valid = rows[m_indices[rows] >= 0]
+    tolerance_check(bf16_bits_to_f32(out[valid]), bf16_bits_to_f32(ref[valid]), "contig")
+    pad = np.nonzero(m_indices < 0)[0]
+    assert np.all(out[pad] == sent)
+
+
+def test_masked_full_size_graph_sampled():
+    w = wl.WORKLOADS["masked"]
+    x, wt, masked_m = wl.masked_inputs(w)
+    ld = oracle.round_up(w.max_m, 4)
+    a = np.empty((w.G, w.max_m, w.K), np.uint8)
+    sfa = np.zeros((w.G, w.K // QB, ld), np.float32)
+    for e in range(w.G):
+        a[e], sfa[e] = oracle.quant_act_1x128(x[e])
+    b, sfb = oracle.quant_weight_128x128(wt)
+    ta, tsa, tb, tsb = dev(a), dev(sfa), dev(b), dev(sfb)
+    mm = dev(masked_m)
+    sent = wl.SENTINEL_BF16
+    d = torch.full((w.G, w.max_m, w.N), sent, dtype=torch.int16, device="cuda")
+    # the launch is CUDA-graph captured, as the workload requires
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        dg.dg_fp8_grouped_masked(ta, tsa, tb, tsb, mm, d.view(torch.bfloat16))
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        dg.dg_fp8_grouped_masked(ta, tsa, tb, tsb, mm, d.view(torch.bfloat16))
+    d.fill_(sent)
+    graph.replay()
+    out = bits(d.view(torch.bfloat16))
+    for e in range(w.G):
+        v = int(masked_m[e])
+        assert np.all(out[e, v:] == sent), f"expert {e} wrote rows beyond masked_m"
+        if v == 0:
+            continue
+        rows = wl.sample_rows(v, 6, w.seed + e, must=[0, v - 1])
+        ref = oracle.gemm_nt(a[e], sfa[e], b[e], sfb[e], rows=rows)
+        tolerance_check(bf16_bits_to_f32(out[e, rows]), bf16_bits_to_f32(ref[rows]), f"masked expert {e}")

@@ -21,7 +21,7 @@ def built():
     dg.dg_read_device_status()
 
 
-@pytest.fixture(params=[128, 192], ids=["bn128", "bn192"])
+@pytest.fixture(params=[96, 128, 192], ids=["bn96", "bn128", "bn192"])
 def tile_n(request, monkeypatch):
     """Runs the test with each compiled tile width (the plan's choice is
     pinned through DG_FORCE_BN)."""
