@@ -152,6 +152,32 @@ def algorithmic_bytes(w: wl.Workload):
     return useful * K + experts * N * K + useful * KB * 4 + experts * NB * KB * 4 + useful * N * 2
 
 
+# -------------------------------------------------------- ncu traffic ------
+GEMM_SOURCES = ("dg_common.h", "dg_gemm.cu", "dg_ptx.cuh")
+
+
+def measured_traffic(profile: str):
+    """DRAM bytes per launch from a committed ncu summary, if that summary was
+    taken from the kernel as it is now (its source hash matches), else None."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "moe_grouped_gemm_x128_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    fields = {}
+    try:
+        with open(os.path.join(ROOT, "profiles", profile)) as fh:
+            for line in fh:
+                if ":" in line and not line.startswith(("|", "#", " ")):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+    except OSError:
+        return None
+    if fields.get("source_sha256") != h.hexdigest()[:16] or "dram_bytes_per_launch" not in fields:
+        return None
+    return int(fields["dram_bytes_per_launch"])
+
+
 # ------------------------------------------------------------- replicas ----
 def max_over_ranks(value: float, device=None) -> float:
     """The largest value over all ranks (the job's time is its slowest
@@ -380,7 +406,7 @@ def run_gpu(args, w):
     else:
         roof = {"bound": "tensor", "achieved": flops_step / gemm_s / 1e12, "peak": fp8_peak, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = measured_traffic(f"fp8_gemm_{w.name}_M{M}_N{N}_K{K}.md")
     roof["peak_source"] = f"{src} (MEASURED_PEAKS.json; fp8 = bf16 x {FP8_PER_BF16:g})" if src == "measured" \
         else "fallback"
     roof["kernel"] = "fp8_gemm_kernel"
