@@ -473,13 +473,14 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
                 sa3 = load_sa(kb + 4);
                 sb0 = sb1;
                 sb1 = kb + 2 < KB ? __ldg(sfb_row + kb + 2) : 0.0f;
-                // wait until the MMAs of this K block are complete: one thread
-                // polls the barrier, the named barrier releases the other
-                // epilogue threads and shares the outcome
-                bool got = true;
-                if (threadIdx.x == kEpiWarp0 * 32)
-                    got = wait_phase(tfull_bar(buf), tph, abort_flag, status);
-                if (!named_barrier_and(1, kNumEpiWarps * 32, got)) {
+                // wait until the MMAs of this K block are complete: lane 0 of
+                // each warp polls the barrier and shuffles the outcome to its
+                // warp.  No bar.sync / bar.warp.sync here: those order memory,
+                // which would make the scale loads issued ahead complete first.
+                uint32_t got = 1;
+                if (lane == 0)
+                    got = wait_phase(tfull_bar(buf), tph, abort_flag, status) ? 1u : 0u;
+                if (__shfl_sync(0xffffffffu, got, 0) == 0) {
                     ok = false;
                     break;
                 }
@@ -502,8 +503,9 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
                     if (c + 1 < kChunks)
                         tmem_wait_ld16(nxt);
                 }
+                // the warp-collective wait::ld above completed every lane's
+                // loads of this buffer; lane 0 releases it for the warp
                 tc_fence_before();
-                __syncwarp();
                 if (lane == 0)
                     mbar_arrive(tempty_bar(buf));
                 if (++buf == kBufs) {
