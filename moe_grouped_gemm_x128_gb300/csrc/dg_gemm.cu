@@ -63,14 +63,19 @@ struct Roles {
     static constexpr int kThreads = 32 * (kEpiWarp0 + kNumEpiWarps);
 };
 constexpr int kGroupM = 16;                // m-blocks per rasterisation band
+constexpr int kMaxBufs = 5;                // TMEM partial buffers at most (512 columns / BN)
 constexpr int kMaxMaskedGroups = 1024;     // G limit of the masked layout (tile prefix in smem)
 // Pipeline waits give up after this many SM cycles (about 2 s at 2 GHz).
 constexpr long long kWaitTimeoutCycles = 4000000000ll;
 
-template <int BN, int STAGES, int EPI_COLS>
+template <int BN, int STAGES, int EPI_COLS, int KPS>
 struct SmemLayout {
-    static constexpr int kABytes = kBM * kBK;       // 16 KiB
-    static constexpr int kBBytes = BN * kBK;
+    // one ring stage holds KPS consecutive K blocks of A and of B, each a
+    // 128-byte-swizzled [rows][128] tile
+    static constexpr int kASub = kBM * kBK;         // 16 KiB
+    static constexpr int kBSub = BN * kBK;
+    static constexpr int kABytes = KPS * kASub;
+    static constexpr int kBBytes = KPS * kBSub;
     static constexpr int kAOff = 0;
     static constexpr int kBOff = kAOff + STAGES * kABytes;
     // output staging: each epilogue warp owns 32 rows x EPI_COLS bf16, rows
@@ -80,8 +85,8 @@ struct SmemLayout {
     static constexpr int kOutWarpBytes = 32 * kOutRowStride;
     static constexpr int kOutOff = kBOff + STAGES * kBBytes;
     static constexpr int kBarOff = kOutOff + (BN / EPI_COLS) * 4 * kOutWarpBytes;
-    // full[S], empty[S], tfull[4], tempty[4], drain[2]
-    static constexpr int kNumBars = 2 * STAGES + 10;
+    // full[S], empty[S], tfull[kMaxBufs], tempty[kMaxBufs], drain[2]
+    static constexpr int kNumBars = 2 * STAGES + 2 * kMaxBufs + 2;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;   // tmem base, abort flag
     static constexpr int kPrefixOff = kMiscOff + 16;
     static constexpr int kBytes = kPrefixOff + (kMaxMaskedGroups + 1) * 4;
@@ -207,24 +212,27 @@ struct Sched {
     }
 };
 
-template <int BN, int STAGES, int EPI_COLS>
+template <int BN, int STAGES, int EPI_COLS, int KPS>
 __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const float *__restrict__ sfa, const float *__restrict__ sfb,
                     uint16_t *__restrict__ d, const int32_t *__restrict__ meta, Problem p,
                     unsigned int *status)
 {
-    using L = SmemLayout<BN, STAGES, EPI_COLS>;
+    using L = SmemLayout<BN, STAGES, EPI_COLS, KPS>;
     constexpr int kNumEpiWarps = Roles<BN, EPI_COLS>::kNumEpiWarps;
-    // TMEM partial buffers: as many 128 x BN fp32 buffers as fit (max 4)
-    constexpr int kBufs = (4 * BN <= 512) ? 4 : (512 / BN);
+    // TMEM partial buffers: as many 128 x BN fp32 buffers as fit in 512 columns
+    constexpr int kBufs = (512 / BN < kMaxBufs) ? 512 / BN : kMaxBufs;
     constexpr uint32_t kTmemCols = (kBufs * BN <= 32)    ? 32
                                    : (kBufs * BN <= 64)  ? 64
                                    : (kBufs * BN <= 128) ? 128
                                    : (kBufs * BN <= 256) ? 256
                                                          : 512;
     constexpr int kCols = EPI_COLS;                    // columns per epilogue warpgroup
-    constexpr int kChunks = kCols / 16;                // 16-column TMEM loads per K block
+    // TMEM loads of kW columns; 32 where the registers allow (one load and one
+    // wait per K block at 32 columns a warpgroup)
+    constexpr int kW = (BN == 192) ? 16 : 32;
+    constexpr int kChunks = kCols / kW;                // TMEM loads per K block
     constexpr uint32_t kStageTx = L::kABytes + L::kBBytes;
     constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, BN);
     static_assert(BN % EPI_COLS == 0 && EPI_COLS % 16 == 0 && BN <= 256, "BN must be a multiple of EPI_COLS up to 256");
@@ -238,8 +246,8 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 4 + b); };
-    auto drain_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 8 + i); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + kMaxBufs + b); };
+    auto drain_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 2 * kMaxBufs + i); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::kMiscOff + 4);
     int *prefix = reinterpret_cast<int *>(smem + L::kPrefixOff);
@@ -247,9 +255,10 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int KB = p.K / kBK;
+    const int KP = (KB + KPS - 1) / KPS;   // ring stages (load units) per tile
     const int NBs = (p.N + 127) / 128;   // 128-column scale blocks of B
 
-    // --------------------------------------------- setup (no global memory)
+    // ------------------------------------------------------------------ setup
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
@@ -267,7 +276,8 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
         tma_prefetch_desc(&tmap_a);
         tma_prefetch_desc(&tmap_b);
     }
-    if (warp == 0) {
+    if (warp == 2) {
+        // TMEM is allocated by warp 2 while thread 0 sets up the barriers
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -278,86 +288,121 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     sch.n_blocks = (p.N + BN - 1) / BN;
     sch.G = p.G;
     sch.prefix = prefix;
-    if (p.layout == DG_LAYOUT_MASKED) {
-        // per-expert tile counts from masked_m, read on the device
-        if (warp == 1) {
-            const int max_mb = (p.M + kBM - 1) / kBM;
-            int running = 0;
-            for (int base = 0; base < p.G; base += 32) {
-                const int g = base + lane;
-                int cnt = 0;
-                if (g < p.G) {
-                    int mm = meta[g];
-                    if (mm < 0 || mm > p.M) {
-                        raise_status(status, DG_DEVFLAG_MASKED_M_CLAMPED);
-                        mm = mm < 0 ? 0 : p.M;
-                    }
-                    cnt = min((mm + kBM - 1) / kBM, max_mb) * sch.n_blocks;
+    sch.m_blocks = (p.layout == DG_LAYOUT_MASKED) ? 0 : (p.M + kBM - 1) / kBM;
+    sch.num_tiles = sch.m_blocks * sch.n_blocks;   // masked: set from the prefix below
+
+    // TMA producer state (thread 0): a cursor over this CTA's (tile, K block)
+    // load units and the ring position
+    int p_stage = 0;
+    uint32_t p_phase = 0;
+    uint32_t pending = 0;        // stages with a copy whose consumption was not yet observed
+    uint32_t pending_par = 0;    // full-barrier parity of each pending copy
+    int p_t = blockIdx.x;
+    int p_u = 0;                 // load unit (group of KPS K blocks) within the tile
+    bool p_have = false;
+    TileInfo p_ti{};
+    // moves the cursor to the next unit to load; false when there is none
+    auto p_next = [&]() -> bool {
+        for (;;) {
+            if (!p_have) {
+                if (p_t >= sch.num_tiles)
+                    return false;
+                p_ti = sch.tile(p_t, p, meta);
+                if (p_ti.skip) {
+                    p_t += gridDim.x;
+                    continue;
                 }
-                int incl = cnt;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o)
-                        incl += v;
-                }
-                if (g < p.G)
-                    prefix[g + 1] = running + incl;
-                running += __shfl_sync(0xffffffffu, incl, 31);
+                p_have = true;
+                p_u = 0;
             }
-            if (lane == 0)
-                prefix[0] = 0;
+            if (p_u < KP)
+                return true;
+            p_have = false;
+            p_t += gridDim.x;
         }
-        sch.m_blocks = 0;
-    } else {
-        sch.m_blocks = (p.M + kBM - 1) / kBM;
+    };
+    // issues the loads of the unit under the cursor into the current stage
+    auto p_issue = [&]() {
+        const uint32_t fb = full_bar(p_stage);
+        mbar_arrive_expect_tx(fb, kStageTx);
+        const uint32_t a_dst = sbase + L::kAOff + p_stage * L::kABytes;
+        const uint32_t b_dst = sbase + L::kBOff + p_stage * L::kBBytes;
+        // tensor maps view K as (128 bytes) x (K blocks); a box covers KPS
+        // K blocks (past the last one it is zero-filled)
+        const int kb0 = p_u * KPS;
+        if (p.layout == DG_LAYOUT_DENSE) {
+            tma_load_3d(a_dst, &tmap_a, fb, 0, p_ti.m0, kb0);
+            tma_load_3d(b_dst, &tmap_b, fb, 0, p_ti.n0, kb0);
+        } else if (p.layout == DG_LAYOUT_CONTIGUOUS) {
+            tma_load_3d(a_dst, &tmap_a, fb, 0, p_ti.m0, kb0);
+            tma_load_4d(b_dst, &tmap_b, fb, 0, p_ti.n0, kb0, p_ti.g);
+        } else {
+            tma_load_4d(a_dst, &tmap_a, fb, 0, p_ti.m0, kb0, p_ti.g);
+            tma_load_4d(b_dst, &tmap_b, fb, 0, p_ti.n0, kb0, p_ti.g);
+        }
+        pending |= 1u << p_stage;
+        pending_par = (pending_par & ~(1u << p_stage)) | (p_phase << p_stage);
+        ++p_u;
+        if (++p_stage == STAGES) {
+            p_stage = 0;
+            p_phase ^= 1u;
+        }
+    };
+    if (threadIdx.x == 0 && p.layout != DG_LAYOUT_MASKED) {
+        // the ring is empty: fill it before the CTA barrier, so that the first
+        // copies overlap the TMEM allocation and the other warps' set-up
+        for (int i = 0; i < STAGES && p_next(); ++i)
+            p_issue();
+    }
+
+    if (p.layout == DG_LAYOUT_MASKED && warp == 1) {
+        // per-expert tile counts from masked_m, read on the device
+        const int max_mb = (p.M + kBM - 1) / kBM;
+        int running = 0;
+        for (int base = 0; base < p.G; base += 32) {
+            const int g = base + lane;
+            int cnt = 0;
+            if (g < p.G) {
+                int mm = meta[g];
+                if (mm < 0 || mm > p.M) {
+                    raise_status(status, DG_DEVFLAG_MASKED_M_CLAMPED);
+                    mm = mm < 0 ? 0 : p.M;
+                }
+                cnt = min((mm + kBM - 1) / kBM, max_mb) * sch.n_blocks;
+            }
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o)
+                    incl += v;
+            }
+            if (g < p.G)
+                prefix[g + 1] = running + incl;
+            running += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0)
+            prefix[0] = 0;
     }
     tc_fence_before();
+    __syncwarp();
     __syncthreads();
     tc_fence_after();
-    sch.num_tiles = (p.layout == DG_LAYOUT_MASKED) ? prefix[p.G] : sch.m_blocks * sch.n_blocks;
+    if (p.layout == DG_LAYOUT_MASKED)
+        sch.num_tiles = prefix[p.G];
     const uint32_t tmem_base = *tmem_slot;
     if (warp < kEpiWarp0) {
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t pending = 0;        // stages with a copy whose consumption was not yet observed
-            uint32_t pending_par = 0;    // full-barrier parity of each pending copy
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < sch.num_tiles; t += gridDim.x) {
-                const TileInfo ti = sch.tile(t, p, meta);
-                if (ti.skip)
-                    continue;
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, status)) {
-                        ok = false;
-                        break;
-                    }
-                    pending &= ~(1u << stage);
-                    const uint32_t fb = full_bar(stage);
-                    mbar_arrive_expect_tx(fb, kStageTx);
-                    const uint32_t a_dst = sbase + L::kAOff + stage * L::kABytes;
-                    const uint32_t b_dst = sbase + L::kBOff + stage * L::kBBytes;
-                    const int k0 = kb * kBK;
-                    if (p.layout == DG_LAYOUT_DENSE) {
-                        tma_load_2d(a_dst, &tmap_a, fb, k0, ti.m0);
-                        tma_load_2d(b_dst, &tmap_b, fb, k0, ti.n0);
-                    } else if (p.layout == DG_LAYOUT_CONTIGUOUS) {
-                        tma_load_2d(a_dst, &tmap_a, fb, k0, ti.m0);
-                        tma_load_3d(b_dst, &tmap_b, fb, k0, ti.n0, ti.g);
-                    } else {
-                        tma_load_3d(a_dst, &tmap_a, fb, k0, ti.m0, ti.g);
-                        tma_load_3d(b_dst, &tmap_b, fb, k0, ti.n0, ti.g);
-                    }
-                    pending |= 1u << stage;
-                    pending_par = (pending_par & ~(1u << stage)) | (phase << stage);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+            while (p_next()) {
+                if (!wait_phase(empty_bar(p_stage), p_phase ^ 1u, abort_flag, status)) {
+                    ok = false;
+                    break;
                 }
+                pending &= ~(1u << p_stage);
+                p_issue();
             }
             if (!ok) {
                 // let the copies already issued land before the CTA exits
@@ -368,43 +413,51 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
         }
     } else if (warp == 1 || warp == 2) {
         // ------------------------------------------------------ MMA issuers
-        // Two threads in two warps take alternate K blocks (by a running
+        // Two threads in two warps take alternate ring stages (by a running
         // count over all tiles), so that one's barrier waits and commits
         // overlap the other's MMAs.
         if (lane == 0) {
             const uint32_t me = static_cast<uint32_t>(warp - 1);
             const uint64_t desc_a0 = smem_desc_sw128(sbase + L::kAOff);
             const uint64_t desc_b0 = smem_desc_sw128(sbase + L::kBOff);
-            uint32_t gkb = 0;
+            uint32_t gu = 0;       // load units over all tiles: the ring position
+            uint32_t tiles = 0;    // tiles done: K block gkb = tiles * KB + kb selects the TMEM buffer
             bool ok = true;
             for (int t = blockIdx.x; ok && t < sch.num_tiles; t += gridDim.x) {
                 const TileInfo ti = sch.tile(t, p, meta);
                 if (ti.skip)
                     continue;
-                for (int kb = 0; kb < KB; ++kb, ++gkb) {
-                    if ((gkb % kIssuers) != me)
+                for (int u = 0; ok && u < KP; ++u, ++gu) {
+                    if ((gu % kIssuers) != me)
                         continue;
-                    const uint32_t stage = gkb % STAGES;
-                    const uint32_t phase = (gkb / STAGES) & 1u;
-                    const uint32_t buf = gkb % kBufs;
-                    const uint32_t tph = (gkb / kBufs) & 1u;
-                    if (!wait_phase(tempty_bar(buf), tph ^ 1u, abort_flag, status) ||
-                        !wait_phase(full_bar(stage), phase, abort_flag, status)) {
-                        ok = false;
-                        break;
+                    const uint32_t stage = gu % STAGES;
+                    const uint32_t phase = (gu / STAGES) & 1u;
+                    const int kb0 = u * KPS;
+                    const int nkb = min(KPS, KB - kb0);
+                    for (int j = 0; j < nkb; ++j) {
+                        const uint32_t gkb = tiles * static_cast<uint32_t>(KB) + static_cast<uint32_t>(kb0 + j);
+                        const uint32_t buf = gkb % kBufs;
+                        const uint32_t tph = (gkb / kBufs) & 1u;
+                        if (!wait_phase(tempty_bar(buf), tph ^ 1u, abort_flag, status) ||
+                            (j == 0 && !wait_phase(full_bar(stage), phase, abort_flag, status))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t da = desc_a0 + static_cast<uint64_t>((stage * L::kABytes + j * L::kASub) >> 4);
+                        const uint64_t db = desc_b0 + static_cast<uint64_t>((stage * L::kBBytes + j * L::kBSub) >> 4);
+                        const uint32_t d_tmem = tmem_base + buf * BN;
+                        // 4 MMAs of K = 32 bytes; each step advances the start address by 32 B
+                        mma_f8f6f4<false>(d_tmem, da, db, kIdesc);
+                        mma_f8f6f4<true>(d_tmem, da + 2, db + 2, kIdesc);
+                        mma_f8f6f4<true>(d_tmem, da + 4, db + 4, kIdesc);
+                        mma_f8f6f4<true>(d_tmem, da + 6, db + 6, kIdesc);
+                        mma_commit(tfull_bar(buf));
                     }
-                    tc_fence_after();
-                    const uint64_t da = desc_a0 + static_cast<uint64_t>((stage * L::kABytes) >> 4);
-                    const uint64_t db = desc_b0 + static_cast<uint64_t>((stage * L::kBBytes) >> 4);
-                    const uint32_t d_tmem = tmem_base + buf * BN;
-                    // 4 MMAs of K = 32 bytes; each step advances the start address by 32 B
-                    mma_f8f6f4<false>(d_tmem, da, db, kIdesc);
-                    mma_f8f6f4<true>(d_tmem, da + 2, db + 2, kIdesc);
-                    mma_f8f6f4<true>(d_tmem, da + 4, db + 4, kIdesc);
-                    mma_f8f6f4<true>(d_tmem, da + 6, db + 6, kIdesc);
-                    mma_commit(empty_bar(stage));
-                    mma_commit(tfull_bar(buf));
+                    if (ok)
+                        mma_commit(empty_bar(stage));
                 }
+                ++tiles;
             }
             // every MMA this thread issued has completed once this barrier flips
             mma_commit(drain_bar(me));
@@ -444,73 +497,99 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
                     }
                 }
             }
-            // this row's activation scales: sfa[kb][m] (masked: per expert),
-            // read ahead four K blocks; rows outside A read nothing
-            const bool row_in = ti.m0 + r < p.M;
+            // This row's activation scales sfa[kb][m] (masked: per expert) and
+            // the scales sfb[nb][kb] of the 128-column block of B holding this
+            // warpgroup's columns are read kAhead K blocks ahead into register
+            // rings indexed by kb % kAhead.  The K loop is unrolled by kAhead,
+            // so every ring slot is one fixed register, written by its load and
+            // read kAhead blocks later: rotating the values through moves would
+            // make each move wait for the load still in flight.
+            constexpr int kAhead = (BN == 192) ? 2 : 4;   // 512 threads x 128 registers at 192
+            const bool row_in = ti.m0 + r < p.M;   // rows outside A read nothing
             const float *sfa_row = sfa + (p.layout == DG_LAYOUT_MASKED ? static_cast<size_t>(ti.g) * KB * p.ldsfa : 0) +
                                    ti.m0 + r;
+            const int nb = min((ti.n0 + c0) >> 7, NBs - 1);
+            const float *sfb_row = sfb + (static_cast<size_t>(ti.g) * NBs + nb) * KB;
             auto load_sa = [&](int kb) -> float {
                 return (row_in && kb < KB) ? __ldg(sfa_row + static_cast<size_t>(kb) * p.ldsfa) : 0.0f;
             };
-            float sa0 = load_sa(0), sa1 = load_sa(1), sa2 = load_sa(2), sa3 = load_sa(3);
-            // the 128-column scale block of B holding this warpgroup's columns
-            const int nb = min((ti.n0 + c0) >> 7, NBs - 1);
-            const float *sfb_row = sfb + (static_cast<size_t>(ti.g) * NBs + nb) * KB;
-            float sb0 = __ldg(sfb_row), sb1 = KB > 1 ? __ldg(sfb_row + 1) : 0.0f;
+            auto load_sb = [&](int kb) -> float { return kb < KB ? __ldg(sfb_row + kb) : 0.0f; };
+            float sa_r[kAhead], sb_r[kAhead];
+#pragma unroll
+            for (int j = 0; j < kAhead; ++j) {
+                sa_r[j] = load_sa(j);
+                sb_r[j] = load_sb(j);
+            }
 
             float2 acc[kCols / 2];
 #pragma unroll
             for (int j = 0; j < kCols / 2; ++j)
                 acc[j] = make_float2(0.0f, 0.0f);
 
-            for (int kb = 0; kb < KB; ++kb) {
-                // fp32 product of the two scales, rounded once
-                const float s = sa0 * sb0;
-                const float2 s2 = make_float2(s, s);
-                sa0 = sa1;
-                sa1 = sa2;
-                sa2 = sa3;
-                sa3 = load_sa(kb + 4);
-                sb0 = sb1;
-                sb1 = kb + 2 < KB ? __ldg(sfb_row + kb + 2) : 0.0f;
-                // wait until the MMAs of this K block are complete: lane 0 of
-                // each warp polls the barrier and shuffles the outcome to its
-                // warp.  No bar.sync / bar.warp.sync here: those order memory,
-                // which would make the scale loads issued ahead complete first.
-                uint32_t got = 1;
-                if (lane == 0)
-                    got = wait_phase(tfull_bar(buf), tph, abort_flag, status) ? 1u : 0u;
-                if (__shfl_sync(0xffffffffu, got, 0) == 0) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t t_buf = t_lane + buf * BN;
-                uint32_t v0[16], v1[16];
-                tmem_ld16(t_buf, v0);
-                tmem_wait_ld16(v0);
+            for (int kb0 = 0; ok && kb0 < KB; kb0 += kAhead) {
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c) {
-                    uint32_t(&cur)[16] = (c & 1) ? v1 : v0;
-                    uint32_t(&nxt)[16] = (c & 1) ? v0 : v1;
-                    if (c + 1 < kChunks)
-                        tmem_ld16(t_buf + (c + 1) * 16, nxt);
+                for (int j = 0; j < kAhead; ++j) {
+                    const int kb = kb0 + j;
+                    if (kb >= KB)
+                        break;
+                    // fp32 product of the two scales, rounded once
+                    const float s = sa_r[j] * sb_r[j];
+                    const float2 s2 = make_float2(s, s);
+                    sa_r[j] = load_sa(kb + kAhead);
+                    sb_r[j] = load_sb(kb + kAhead);
+                    // wait until the MMAs of this K block are complete: lane 0 of
+                    // each warp polls the barrier and shuffles the outcome to its
+                    // warp.  No bar.sync / bar.warp.sync here: those order memory,
+                    // which would make the scale loads issued ahead complete first.
+                    uint32_t got = 1;
+                    if (lane == 0)
+                        got = wait_phase(tfull_bar(buf), tph, abort_flag, status) ? 1u : 0u;
+                    if (__shfl_sync(0xffffffffu, got, 0) == 0) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t t_buf = t_lane + buf * BN;
+                    uint32_t v0[kW], v1[kW];
+                    auto ld = [&](uint32_t addr, uint32_t(&r)[kW]) {
+                        if constexpr (kW == 32)
+                            tmem_ld32(addr, r);
+                        else
+                            tmem_ld16(addr, r);
+                    };
+                    auto wait = [&](uint32_t(&r)[kW]) {
+                        if constexpr (kW == 32)
+                            tmem_wait_ld32(r);
+                        else
+                            tmem_wait_ld16(r);
+                    };
+                    ld(t_buf, v0);
+                    wait(v0);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        acc[c * 8 + j] =
-                            ffma2(make_float2(__uint_as_float(cur[2 * j]), __uint_as_float(cur[2 * j + 1])), s2,
-                                  acc[c * 8 + j]);
-                    if (c + 1 < kChunks)
-                        tmem_wait_ld16(nxt);
-                }
-                // the warp-collective wait::ld above completed every lane's
-                // loads of this buffer; lane 0 releases it for the warp
-                tc_fence_before();
-                if (lane == 0)
-                    mbar_arrive(tempty_bar(buf));
-                if (++buf == kBufs) {
-                    buf = 0;
-                    tph ^= 1u;
+                    for (int c = 0; c < kChunks; ++c) {
+                        uint32_t(&cur)[kW] = (c & 1) ? v1 : v0;
+                        uint32_t(&nxt)[kW] = (c & 1) ? v0 : v1;
+                        if (c + 1 < kChunks) {
+                            ld(t_buf + (c + 1) * kW, nxt);
+                        } else {
+                            // every load of this buffer has completed (warp-collective
+                            // wait::ld): lane 0 releases it before the last FMAs
+                            tc_fence_before();
+                            if (lane == 0)
+                                mbar_arrive(tempty_bar(buf));
+                        }
+#pragma unroll
+                        for (int i = 0; i < kW / 2; ++i)
+                            acc[c * (kW / 2) + i] =
+                                ffma2(make_float2(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), s2,
+                                      acc[c * (kW / 2) + i]);
+                        if (c + 1 < kChunks)
+                            wait(nxt);
+                    }
+                    if (++buf == kBufs) {
+                        buf = 0;
+                        tph ^= 1u;
+                    }
                 }
             }
             if (!ok)
@@ -549,9 +628,13 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     }
 
     // ------------------------------------------------------------- teardown
+    // Lane 0 of warps 0-2 ran its role alone: reconverge each warp before the
+    // CTA barrier (bar.sync counts a warp as arrived when any of its lanes
+    // executes it, so a diverged warp would let the barrier open early).
     tc_fence_before();
+    __syncwarp();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
     }
@@ -575,12 +658,16 @@ struct Plan {
 // SM count.
 struct TileCfg {
     int bn;
-    int stages;
-    int epi_cols;
+    int stages;     // ring stages
+    int epi_cols;   // columns per epilogue warpgroup
+    int kps;        // K blocks per ring stage (one TMA box per operand)
 };
-constexpr TileCfg kCfg96{96, 6, 32};
-constexpr TileCfg kCfg128{128, 5, 64};
-constexpr TileCfg kCfg192{192, 4, 64};
+// A TMA copy costs the SM a roughly fixed issue slot whatever its size, so
+// the narrow tile streams two K blocks per box; at 128 x 192 the copies are
+// large enough already and shared memory holds four one-block stages.
+constexpr TileCfg kCfg96{96, 3, 32, 2};
+constexpr TileCfg kCfg128{128, 5, 64, 1};
+constexpr TileCfg kCfg192{192, 4, 64, 1};
 
 int forced_bn()
 {
@@ -592,9 +679,9 @@ int forced_bn()
 
 int smem_for(int bn)
 {
-    return bn == 192 ? SmemLayout<192, kCfg192.stages, kCfg192.epi_cols>::kAlloc
-           : bn == 96 ? SmemLayout<96, kCfg96.stages, kCfg96.epi_cols>::kAlloc
-                      : SmemLayout<128, kCfg128.stages, kCfg128.epi_cols>::kAlloc;
+    return bn == 192 ? SmemLayout<192, kCfg192.stages, kCfg192.epi_cols, kCfg192.kps>::kAlloc
+           : bn == 96 ? SmemLayout<96, kCfg96.stages, kCfg96.epi_cols, kCfg96.kps>::kAlloc
+                      : SmemLayout<128, kCfg128.stages, kCfg128.epi_cols, kCfg128.kps>::kAlloc;
 }
 
 Plan make_plan(int layout, int M, int N, int K, int G, int num_sms)
@@ -654,31 +741,38 @@ dg_status_t launch(int layout, const uint8_t *a, const float *sfa, const uint8_t
     const Plan pl = make_plan(layout, M, N, K, G, info.sm_count);
     const int ldsfa = round_up(M, 4);
 
+    // Tensor maps view each K-major operand as [..][rows][K/128][128 bytes]:
+    // dim 0 is the 128-byte row segment of one K block, dim 1 the row (stride
+    // K), dim 2 the K block (stride 128) and dim 3, for the grouped operands,
+    // the expert.  A box is 128 bytes x rows x KPS K blocks.
+    const int kps = pl.bn == 192 ? kCfg192.kps : pl.bn == 96 ? kCfg96.kps : kCfg128.kps;
+    const uint64_t KB = static_cast<uint64_t>(K / kBK);
     CUtensorMap ta, tb;
     {
         // A: E4M3 [rows][K] (dense / contiguous) or [G][max_m][K] (masked)
-        const uint64_t dims3[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint64_t>(G)};
-        const uint64_t strides[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(K) * M};
-        const uint32_t box[3] = {kBK, kBM, 1};
-        st = encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, layout == DG_LAYOUT_MASKED ? 3 : 2, a, dims3,
+        const uint64_t dims[4] = {static_cast<uint64_t>(kBK), static_cast<uint64_t>(M), KB, static_cast<uint64_t>(G)};
+        const uint64_t strides[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(kBK),
+                                     static_cast<uint64_t>(K) * M};
+        const uint32_t box[4] = {kBK, kBM, static_cast<uint32_t>(kps), 1};
+        st = encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, layout == DG_LAYOUT_MASKED ? 4 : 3, a, dims,
                                strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st != DG_OK)
             return st;
     }
     {
         // B: E4M3 [N][K] (dense) or [G][N][K]
-        const int Gb = layout == DG_LAYOUT_DENSE ? 1 : G;
-        const uint64_t dims3[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(Gb)};
-        const uint64_t strides[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(K) * N};
-        const uint32_t box[3] = {kBK, static_cast<uint32_t>(pl.bn), 1};
-        st = encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, layout == DG_LAYOUT_DENSE ? 2 : 3, b, dims3,
+        const uint64_t dims[4] = {static_cast<uint64_t>(kBK), static_cast<uint64_t>(N), KB, static_cast<uint64_t>(G)};
+        const uint64_t strides[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(kBK),
+                                     static_cast<uint64_t>(K) * N};
+        const uint32_t box[4] = {kBK, static_cast<uint32_t>(pl.bn), static_cast<uint32_t>(kps), 1};
+        st = encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, layout == DG_LAYOUT_DENSE ? 3 : 4, b, dims,
                                strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st != DG_OK)
             return st;
     }
-    auto kernel = pl.bn == 192  ? fp8_gemm_kernel<192, kCfg192.stages, kCfg192.epi_cols>
-                  : pl.bn == 96 ? fp8_gemm_kernel<96, kCfg96.stages, kCfg96.epi_cols>
-                                : fp8_gemm_kernel<128, kCfg128.stages, kCfg128.epi_cols>;
+    auto kernel = pl.bn == 192  ? fp8_gemm_kernel<192, kCfg192.stages, kCfg192.epi_cols, kCfg192.kps>
+                  : pl.bn == 96 ? fp8_gemm_kernel<96, kCfg96.stages, kCfg96.epi_cols, kCfg96.kps>
+                                : fp8_gemm_kernel<128, kCfg128.stages, kCfg128.epi_cols, kCfg128.kps>;
     const int threads = pl.bn == 192  ? Roles<192, kCfg192.epi_cols>::kThreads
                         : pl.bn == 96 ? Roles<96, kCfg96.epi_cols>::kThreads
                                       : Roles<128, kCfg128.epi_cols>::kThreads;
