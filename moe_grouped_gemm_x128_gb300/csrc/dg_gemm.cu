@@ -221,13 +221,18 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
 {
     using L = SmemLayout<BN, STAGES, EPI_COLS, KPS>;
     constexpr int kNumEpiWarps = Roles<BN, EPI_COLS>::kNumEpiWarps;
-    // TMEM partial buffers: as many 128 x BN fp32 buffers as fit in 512 columns
-    constexpr int kBufs = (512 / BN < kMaxBufs) ? 512 / BN : kMaxBufs;
-    constexpr uint32_t kTmemCols = (kBufs * BN <= 32)    ? 32
-                                   : (kBufs * BN <= 64)  ? 64
-                                   : (kBufs * BN <= 128) ? 128
-                                   : (kBufs * BN <= 256) ? 256
-                                                         : 512;
+    // TMEM slots: one per ring stage in flight between the MMAs and the
+    // epilogue, each holding the KPS partial products (128 x BN fp32) of one
+    // stage's K blocks; as many as fit in 512 columns.  A barrier handoff costs
+    // a few hundred cycles, so the MMA side signals, and the epilogue releases,
+    // a whole stage at once.
+    constexpr int kSlotCols = KPS * BN;
+    constexpr int kBufs = (512 / kSlotCols < kMaxBufs) ? 512 / kSlotCols : kMaxBufs;
+    constexpr uint32_t kTmemCols = (kBufs * kSlotCols <= 32)    ? 32
+                                   : (kBufs * kSlotCols <= 64)  ? 64
+                                   : (kBufs * kSlotCols <= 128) ? 128
+                                   : (kBufs * kSlotCols <= 256) ? 256
+                                                                : 512;
     constexpr int kCols = EPI_COLS;                    // columns per epilogue warpgroup
     // TMEM loads of kW columns; 32 where the registers allow (one load and one
     // wait per K block at 32 columns a warpgroup)
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, BN);
     static_assert(BN % EPI_COLS == 0 && EPI_COLS % 16 == 0 && BN <= 256, "BN must be a multiple of EPI_COLS up to 256");
     static_assert(128 % kCols == 0, "the columns of one epilogue warpgroup must lie in one 128-column scale block");
-    static_assert(kBufs >= 2, "at least two TMEM partial buffers");
+    static_assert(kBufs >= 2, "at least two TMEM slots");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -421,7 +426,6 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
             const uint64_t desc_a0 = smem_desc_sw128(sbase + L::kAOff);
             const uint64_t desc_b0 = smem_desc_sw128(sbase + L::kBOff);
             uint32_t gu = 0;       // load units over all tiles: the ring position
-            uint32_t tiles = 0;    // tiles done: K block gkb = tiles * KB + kb selects the TMEM buffer
             bool ok = true;
             for (int t = blockIdx.x; ok && t < sch.num_tiles; t += gridDim.x) {
                 const TileInfo ti = sch.tile(t, p, meta);
@@ -432,32 +436,30 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
                         continue;
                     const uint32_t stage = gu % STAGES;
                     const uint32_t phase = (gu / STAGES) & 1u;
+                    const uint32_t slot = gu % kBufs;
+                    const uint32_t sph = (gu / kBufs) & 1u;
                     const int kb0 = u * KPS;
                     const int nkb = min(KPS, KB - kb0);
+                    if (!wait_phase(tempty_bar(slot), sph ^ 1u, abort_flag, status) ||
+                        !wait_phase(full_bar(stage), phase, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                     for (int j = 0; j < nkb; ++j) {
-                        const uint32_t gkb = tiles * static_cast<uint32_t>(KB) + static_cast<uint32_t>(kb0 + j);
-                        const uint32_t buf = gkb % kBufs;
-                        const uint32_t tph = (gkb / kBufs) & 1u;
-                        if (!wait_phase(tempty_bar(buf), tph ^ 1u, abort_flag, status) ||
-                            (j == 0 && !wait_phase(full_bar(stage), phase, abort_flag, status))) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
                         const uint64_t da = desc_a0 + static_cast<uint64_t>((stage * L::kABytes + j * L::kASub) >> 4);
                         const uint64_t db = desc_b0 + static_cast<uint64_t>((stage * L::kBBytes + j * L::kBSub) >> 4);
-                        const uint32_t d_tmem = tmem_base + buf * BN;
+                        // each K block's partial product has its own BN columns of the slot
+                        const uint32_t d_tmem = tmem_base + slot * kSlotCols + j * BN;
                         // 4 MMAs of K = 32 bytes; each step advances the start address by 32 B
                         mma_f8f6f4<false>(d_tmem, da, db, kIdesc);
                         mma_f8f6f4<true>(d_tmem, da + 2, db + 2, kIdesc);
                         mma_f8f6f4<true>(d_tmem, da + 4, db + 4, kIdesc);
                         mma_f8f6f4<true>(d_tmem, da + 6, db + 6, kIdesc);
-                        mma_commit(tfull_bar(buf));
                     }
-                    if (ok)
-                        mma_commit(empty_bar(stage));
+                    mma_commit(tfull_bar(slot));
+                    mma_commit(empty_bar(stage));
                 }
-                ++tiles;
             }
             // every MMA this thread issued has completed once this barrier flips
             mma_commit(drain_bar(me));
@@ -505,6 +507,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
             // read kAhead blocks later: rotating the values through moves would
             // make each move wait for the load still in flight.
             constexpr int kAhead = (BN == 192) ? 2 : 4;   // 512 threads x 128 registers at 192
+            static_assert(kAhead % KPS == 0, "the unrolled K loop must cover whole ring stages");
             const bool row_in = ti.m0 + r < p.M;   // rows outside A read nothing
             const float *sfa_row = sfa + (p.layout == DG_LAYOUT_MASKED ? static_cast<size_t>(ti.g) * KB * p.ldsfa : 0) +
                                    ti.m0 + r;
@@ -537,19 +540,24 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
                     const float2 s2 = make_float2(s, s);
                     sa_r[j] = load_sa(kb + kAhead);
                     sb_r[j] = load_sb(kb + kAhead);
-                    // wait until the MMAs of this K block are complete: lane 0 of
-                    // each warp polls the barrier and shuffles the outcome to its
-                    // warp.  No bar.sync / bar.warp.sync here: those order memory,
-                    // which would make the scale loads issued ahead complete first.
-                    uint32_t got = 1;
-                    if (lane == 0)
-                        got = wait_phase(tfull_bar(buf), tph, abort_flag, status) ? 1u : 0u;
-                    if (__shfl_sync(0xffffffffu, got, 0) == 0) {
-                        ok = false;
-                        break;
+                    const int jj = j % KPS;                       // K block within its ring stage
+                    const bool last_of_slot = (jj == KPS - 1) || (kb == KB - 1);
+                    if (jj == 0) {
+                        // wait until the MMAs of this stage are complete: lane 0
+                        // of each warp polls the barrier and shuffles the outcome
+                        // to its warp.  No bar.sync / bar.warp.sync here: those
+                        // order memory, which would make the scale loads issued
+                        // ahead complete first.
+                        uint32_t got = 1;
+                        if (lane == 0)
+                            got = wait_phase(tfull_bar(buf), tph, abort_flag, status) ? 1u : 0u;
+                        if (__shfl_sync(0xffffffffu, got, 0) == 0) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
                     }
-                    tc_fence_after();
-                    const uint32_t t_buf = t_lane + buf * BN;
+                    const uint32_t t_buf = t_lane + buf * kSlotCols + jj * BN;
                     uint32_t v0[kW], v1[kW];
                     auto ld = [&](uint32_t addr, uint32_t(&r)[kW]) {
                         if constexpr (kW == 32)
@@ -571,8 +579,8 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
                         uint32_t(&nxt)[kW] = (c & 1) ? v0 : v1;
                         if (c + 1 < kChunks) {
                             ld(t_buf + (c + 1) * kW, nxt);
-                        } else {
-                            // every load of this buffer has completed (warp-collective
+                        } else if (last_of_slot) {
+                            // every load of this slot has completed (warp-collective
                             // wait::ld): lane 0 releases it before the last FMAs
                             tc_fence_before();
                             if (lane == 0)
@@ -586,7 +594,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
                         if (c + 1 < kChunks)
                             wait(nxt);
                     }
-                    if (++buf == kBufs) {
+                    if (last_of_slot && ++buf == kBufs) {
                         buf = 0;
                         tph ^= 1u;
                     }
