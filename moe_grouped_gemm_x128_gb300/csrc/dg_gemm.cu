@@ -243,6 +243,9 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     static_assert(BN % EPI_COLS == 0 && EPI_COLS % 16 == 0 && BN <= 256, "BN must be a multiple of EPI_COLS up to 256");
     static_assert(128 % kCols == 0, "the columns of one epilogue warpgroup must lie in one 128-column scale block");
     static_assert(kBufs >= 2, "at least two TMEM slots");
+    // issuers alternate stages, so slot s is always written by issuer s % 2 and
+    // each thread waits only for its own slot's previous release
+    static_assert(kBufs % kIssuers == 0, "each TMEM slot must belong to one issuer");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -393,6 +396,11 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     __syncwarp();
     __syncthreads();
     tc_fence_after();
+    // a kernel launched after this one with programmatic serialisation (the
+    // activation quantiser of the next step) may be placed now; it waits for
+    // this grid to complete before touching memory
+    if (threadIdx.x == 0)
+        griddep_launch_dependents();
     if (p.layout == DG_LAYOUT_MASKED)
         sch.num_tiles = prefix[p.G];
     const uint32_t tmem_base = *tmem_slot;
@@ -440,6 +448,11 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
                     const uint32_t sph = (gu / kBufs) & 1u;
                     const int kb0 = u * KPS;
                     const int nkb = min(KPS, KB - kb0);
+                    // The slot first, then the data.  A stage's previous use may
+                    // belong to the other issuer; once the epilogue has released
+                    // this slot's previous use, every earlier stage has been
+                    // consumed, so the full barrier cannot be two phases behind
+                    // (a parity test could not tell those apart).
                     if (!wait_phase(tempty_bar(slot), sph ^ 1u, abort_flag, status) ||
                         !wait_phase(full_bar(stage), phase, abort_flag, status)) {
                         ok = false;
@@ -670,9 +683,11 @@ struct TileCfg {
     int epi_cols;   // columns per epilogue warpgroup
     int kps;        // K blocks per ring stage (one TMA box per operand)
 };
-// A TMA copy costs the SM a roughly fixed issue slot whatever its size, so
-// the narrow tile streams two K blocks per box; at 128 x 192 the copies are
-// large enough already and shared memory holds four one-block stages.
+// A TMA copy costs its SM a slot of a few hundred cycles plus the bytes, so
+// the 128 x 96 tile streams two K blocks per box (and hands them to the
+// epilogue as one TMEM slot).  At 128 x 192 two-block stages leave room for
+// two stages and TMEM for two one-block slots, which needs a single issuer:
+// measured slower than four one-block stages with two issuers.
 constexpr TileCfg kCfg96{96, 3, 32, 2};
 constexpr TileCfg kCfg128{128, 5, 64, 1};
 constexpr TileCfg kCfg192{192, 4, 64, 1};
