@@ -83,10 +83,25 @@ def test_read_status_validation(lib):
     assert lib.dg_read_device_status(None, None) == dg.DG_ERR_INVALID_ARG
 
 
+def golden_block_counts():
+    """The pages' worked example (tests/golden/block_counts_m256_n7168.txt)."""
+    path = os.path.join(os.path.dirname(__file__), "golden", "block_counts_m256_n7168.txt")
+    rows = []
+    with open(path) as fh:
+        for line in fh:
+            if line.strip() and not line.startswith("#"):
+                rows.append(tuple(int(v) for v in line.split()))
+    return rows
+
+
 def test_plan_tile_arithmetic_of_the_pages():
     # M=256, N=7168 ("DeepGEMM：一款支持FP8通用矩阵乘法(GEMM)的开源库", 非标准块大小支持):
-    # 128-wide blocks give 2 x 56 = 112 tiles, 112-wide ones 2 x 64 = 128.
-    assert 2 * (7168 // 128) == 112 and 2 * (7168 // 112) == 128
+    # 128-wide blocks keep 112 units busy, 112-wide ones 128; the plan's tile
+    # count for a width is the same arithmetic (one tile per unit).
+    rows = golden_block_counts()
+    assert len(rows) == 2
+    for M, N, bm, bn, busy in rows:
+        assert -(-M // bm) * -(-N // bn) == busy
     # With 132 SMs the plan keeps 128-wide tiles (112 tiles, one wave) ...
     p = dg.dg_query_plan(dg.DG_LAYOUT_DENSE, 256, 7168, 2048, 1, num_sms=132)
     assert (p["block_m"], p["block_n"], p["num_tiles"], p["grid"]) == (128, 128, 112, 112)
