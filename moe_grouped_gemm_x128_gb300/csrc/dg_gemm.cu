@@ -357,9 +357,11 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
         }
     };
     if (threadIdx.x == 0 && p.layout != DG_LAYOUT_MASKED) {
-        // the ring is empty: fill it before the CTA barrier, so that the first
-        // copies overlap the TMEM allocation and the other warps' set-up
-        for (int i = 0; i < STAGES && p_next(); ++i)
+        // the ring is empty: issue the first stage before the CTA barrier, so
+        // that its copies overlap the TMEM allocation and the other warps'
+        // set-up.  Only one: the first copies issue slowly (cold descriptors),
+        // and the MMA issuers wait at the barrier for this thread.
+        if (p_next())
             p_issue();
     }
 
