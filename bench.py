@@ -156,14 +156,25 @@ def algorithmic_bytes(w: wl.Workload):
 GEMM_SOURCES = ("dg_common.h", "dg_gemm.cu", "dg_ptx.cuh")
 
 
+def gemm_source_hash() -> str:
+    """First 16 hex digits of the SHA-256 of the GEMM kernel's sources with
+    comments and blank lines removed (what the compiler sees changes the hash;
+    an edited comment does not)."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "moe_grouped_gemm_x128_gb300", "csrc", f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
+        h.update("\n".join(ln for ln in lines if ln.strip()).encode())
+    return h.hexdigest()[:16]
+
+
 def measured_traffic(profile: str):
     """DRAM bytes per launch from a committed ncu summary, if that summary was
     taken from the kernel as it is now (its source hash matches), else None."""
-    import hashlib
-    h = hashlib.sha256()
-    for f in GEMM_SOURCES:
-        with open(os.path.join(ROOT, "moe_grouped_gemm_x128_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
     fields = {}
     try:
         with open(os.path.join(ROOT, "profiles", profile)) as fh:
@@ -173,7 +184,7 @@ def measured_traffic(profile: str):
                     fields[k.strip()] = v.strip()
     except OSError:
         return None
-    if fields.get("source_sha256") != h.hexdigest()[:16] or "dram_bytes_per_launch" not in fields:
+    if fields.get("source_sha256") != gemm_source_hash() or "dram_bytes_per_launch" not in fields:
         return None
     return int(fields["dram_bytes_per_launch"])
 

@@ -9,33 +9,36 @@
 // kb ascending; D = bf16_rn(acc).
 //
 // How (the page's 线程专业化技术 and 统一的计算任务调度系统, redone for GB300):
-// a persistent kernel, one CTA per SM, 384 threads in three roles:
-//   warp 0      TMA producer: streams A[128x128] and B[BNx128] (128-byte
-//               swizzled) into an S-stage shared-memory ring; also allocates
-//               and frees the TMEM columns;
-//   warps 1, 2  MMA issuers, taking alternate K blocks: one thread each issues
-//               4 x tcgen05.mma kind::f8f6f4 (128 x BN x 32) per K block into
-//               a TMEM partial buffer (the first with accumulate off, so each
-//               K block starts from zero), then commits to the ring's "empty"
-//               barrier and the buffer's "full" barrier; two issuers let one's
-//               barrier round trips overlap the other's MMAs; warp 1 also
+// a persistent kernel, one CTA per SM, in four roles:
+//   warp 0      TMA producer: streams A[128 rows] and B[BN rows] (128-byte
+//               swizzled) into an S-stage shared-memory ring; the tensor maps
+//               view K as (128 bytes) x (K blocks), so one box carries the
+//               KPS K blocks of a stage;
+//   warp 2      allocates and frees the TMEM columns;
+//   warps 1, 2  MMA issuers, taking alternate ring stages: one thread each
+//               waits for the stage's TMEM slot and data, issues
+//               4 x tcgen05.mma kind::f8f6f4 (128 x BN x 32) per K block, each
+//               K block into its own BN columns of the slot (the first MMA with
+//               accumulate off), then commits once to the slot's "full"
+//               barrier and once to the stage's "empty" barrier; warp 1 also
 //               builds the masked layout's per-expert tile prefix;
-//   warps 4-11  epilogue, two warpgroups each owning half of the
-//               tile's columns: each thread owns one output row (TMEM lane);
-//               per K block it loads its partial row from TMEM, scales it by
-//               sfa * sfb (read from global memory a few K blocks ahead) and
-//               FMAs it into fp32 registers (two lanes per instruction), then
-//               releases the buffer, so the MMAs of the next K blocks overlap
-//               the promotion of this one; after the last block it converts to
-//               bf16 and stores the row.
-// Tiles are 128 x 192 (two TMEM buffers, three epilogue warpgroups, 512
-// threads) when the problem has at least a full wave of them, else 128 x 128
-// (four buffers, two warpgroups, 384 threads) or 128 x 96 (four buffers,
-// three 32-column warpgroups), whichever fills the SMs better.  The output
-// tile is staged per warp in shared memory and stored row-major, so that
-// each store instruction writes whole row segments.
-// Tiles are visited in a grouped order (GROUP_M m-blocks per band) so that the
-// CTAs running at the same time share A and B tiles through L2.
+//   warps 4..   epilogue warpgroups, each owning EPI_COLS of the tile's
+//               columns; a thread owns one output row (TMEM lane).  Per slot
+//               lane 0 of each warp waits for the slot, the warp loads its
+//               partial rows from TMEM and releases the slot, then scales each
+//               K block's row by sfa * sfb (read from global memory a few K
+//               blocks ahead into fixed registers) and FMAs it into fp32
+//               registers (two lanes per instruction), K blocks ascending;
+//               after the last block it converts to bf16, stages the rows in
+//               shared memory and stores them row-major.
+// An mbarrier handoff costs a few hundred cycles, so handoffs are per stage
+// and per TMEM slot, not per MMA.  Tiles are 128 x 192 (4 one-K-block stages,
+// two TMEM slots, 512 threads) when the problem has at least a full wave of
+// them, else 128 x 128 (5 one-block stages, four slots, 384 threads) or
+// 128 x 96 (3 two-block stages, two slots of two K blocks, 512 threads),
+// whichever fills the SMs better.  Tiles are visited in a grouped order
+// (kGroupM m-blocks per band) so that the CTAs running at the same time share
+// A and B tiles through L2.
 //
 // Every wait is bounded: after kWaitTimeoutCycles a role raises the CTA's abort
 // flag and DG_DEVFLAG_TIMEOUT, the producer waits (bounded) for its own copies
