@@ -46,7 +46,11 @@ def gpu_dense(a, sfa, b, sfb):
 
 # ------------------------------------------------------------------ dense --
 DENSE_SHAPES = [(128, 256, 512), (1, 128, 128), (129, 136, 384), (300, 392, 640), (513, 1024, 256),
-                (256, 2112, 1024), (1100, 1288, 384), (4224, 1288, 256)]
+                (256, 2112, 1024), (1100, 1288, 384), (4224, 1288, 256),
+                # the narrowest N (one 16-byte row of D), N below one MMA width,
+                # odd K-block counts against two-block stages, and a long K
+                # whose fp32 accumulation is still exact on the exact inputs
+                (3, 8, 256), (130, 24, 640), (257, 200, 1152), (65, 96, 18432)]
 
 
 @pytest.mark.parametrize("M,N,K", DENSE_SHAPES)
@@ -117,7 +121,7 @@ def gpu_contiguous(a, sfa, b, sfb, m_indices):
     return bits(d.view(torch.bfloat16))
 
 
-@pytest.mark.parametrize("G,tokens,N,K", [(4, 700, 256, 512), (8, 1500, 392, 384), (3, 129, 128, 128)])
+@pytest.mark.parametrize("G,tokens,N,K", [(4, 700, 256, 512), (8, 1500, 392, 384), (3, 129, 128, 128), (2, 100, 8, 640)])
 def test_contiguous_exact_bit_identical(G, tokens, N, K, tile_n):
     a, sfa, b, sfb, mi = contiguous_case(G, tokens, N, K, seed=G + tokens, exact=True)
     ref = np.full((a.shape[0], N), wl.SENTINEL_BF16, dtype=np.uint16)
@@ -181,6 +185,7 @@ def gpu_masked(a, sfa, b, sfb, masked_m):
     (4, 256, 256, 512, [0, 1, 255, 256]),
     (3, 200, 392, 384, [200, 129, 128]),
     (2, 64, 128, 128, [64, 3]),
+    (5, 130, 8, 640, [130, 0, 7, 129, 1]),
 ])
 def test_masked_exact_bit_identical(G, max_m, N, K, mm, tile_n):
     a, sfa, b, sfb, masked_m = masked_case(G, max_m, N, K, mm, seed=G * 11 + max_m, exact=True)
