@@ -237,13 +237,15 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
                                    : (kBufs * kSlotCols <= 256) ? 256
                                                                 : 512;
     constexpr int kCols = EPI_COLS;                    // columns per epilogue warpgroup
-    // TMEM loads of kW columns; 32 where the registers allow (one load and one
-    // wait per K block at 32 columns a warpgroup)
-    constexpr int kW = (BN == 192) ? 16 : 32;
+    // TMEM loads of 32 columns (32x32b.x32): one per 32 columns of a K block.
+    // Where registers allow, the next chunk's load overlaps this chunk's FMAs;
+    // at BN = 192 (512 threads, 128 registers) one chunk is held at a time.
+    constexpr int kW = 32;
+    constexpr bool kPrefetchChunk = (BN != 192);
     constexpr int kChunks = kCols / kW;                // TMEM loads per K block
     constexpr uint32_t kStageTx = L::kABytes + L::kBBytes;
     constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, BN);
-    static_assert(BN % EPI_COLS == 0 && EPI_COLS % 16 == 0 && BN <= 256, "BN must be a multiple of EPI_COLS up to 256");
+    static_assert(BN % EPI_COLS == 0 && EPI_COLS % kW == 0 && BN <= 256, "BN must be a multiple of EPI_COLS up to 256");
     static_assert(128 % kCols == 0, "the columns of one epilogue warpgroup must lie in one 128-column scale block");
     static_assert(kBufs >= 2, "at least two TMEM slots");
     // issuers alternate stages, so slot s is always written by issuer s % 2 and
@@ -576,41 +578,47 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
                         tc_fence_after();
                     }
                     const uint32_t t_buf = t_lane + buf * kSlotCols + jj * BN;
-                    uint32_t v0[kW], v1[kW];
-                    auto ld = [&](uint32_t addr, uint32_t(&r)[kW]) {
-                        if constexpr (kW == 32)
-                            tmem_ld32(addr, r);
-                        else
-                            tmem_ld16(addr, r);
-                    };
-                    auto wait = [&](uint32_t(&r)[kW]) {
-                        if constexpr (kW == 32)
-                            tmem_wait_ld32(r);
-                        else
-                            tmem_wait_ld16(r);
-                    };
-                    ld(t_buf, v0);
-                    wait(v0);
+                    uint32_t v0[kW], v1[kPrefetchChunk ? kW : 1];
+                    auto ld = [&](uint32_t addr, uint32_t(&r)[kW]) { tmem_ld32(addr, r); };
+                    auto wait = [&](uint32_t(&r)[kW]) { tmem_wait_ld32(r); };
+                    if constexpr (kPrefetchChunk) {
+                        ld(t_buf, v0);
+                        wait(v0);
 #pragma unroll
-                    for (int c = 0; c < kChunks; ++c) {
-                        uint32_t(&cur)[kW] = (c & 1) ? v1 : v0;
-                        uint32_t(&nxt)[kW] = (c & 1) ? v0 : v1;
-                        if (c + 1 < kChunks) {
-                            ld(t_buf + (c + 1) * kW, nxt);
-                        } else if (last_of_slot) {
-                            // every load of this slot has completed (warp-collective
-                            // wait::ld): lane 0 releases it before the last FMAs
-                            tc_fence_before();
-                            if (lane == 0)
-                                mbar_arrive(tempty_bar(buf));
+                        for (int c = 0; c < kChunks; ++c) {
+                            uint32_t(&cur)[kW] = (c & 1) ? v1 : v0;
+                            uint32_t(&nxt)[kW] = (c & 1) ? v0 : v1;
+                            if (c + 1 < kChunks) {
+                                ld(t_buf + (c + 1) * kW, nxt);
+                            } else if (last_of_slot) {
+                                tc_fence_before();
+                                if (lane == 0)
+                                    mbar_arrive(tempty_bar(buf));
+                            }
+#pragma unroll
+                            for (int i = 0; i < kW / 2; ++i)
+                                acc[c * (kW / 2) + i] =
+                                    ffma2(make_float2(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), s2,
+                                          acc[c * (kW / 2) + i]);
+                            if (c + 1 < kChunks)
+                                wait(nxt);
                         }
+                    } else {
 #pragma unroll
-                        for (int i = 0; i < kW / 2; ++i)
-                            acc[c * (kW / 2) + i] =
-                                ffma2(make_float2(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), s2,
-                                      acc[c * (kW / 2) + i]);
-                        if (c + 1 < kChunks)
-                            wait(nxt);
+                        for (int c = 0; c < kChunks; ++c) {
+                            ld(t_buf + c * kW, v0);
+                            wait(v0);
+                            if (c + 1 == kChunks && last_of_slot) {
+                                tc_fence_before();
+                                if (lane == 0)
+                                    mbar_arrive(tempty_bar(buf));
+                            }
+#pragma unroll
+                            for (int i = 0; i < kW / 2; ++i)
+                                acc[c * (kW / 2) + i] =
+                                    ffma2(make_float2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1])), s2,
+                                          acc[c * (kW / 2) + i]);
+                        }
                     }
                     if (last_of_slot && ++buf == kBufs) {
                         buf = 0;
