@@ -111,11 +111,25 @@ def _check(fn: str, status: int) -> None:
         raise DgError(fn, status, status_string(status))
 
 
+_raw_stream = None
+
+
 def _stream(stream) -> int | None:
+    """The stream handle to launch on: `stream` if given, else the current
+    torch stream of the current device (where the library launches)."""
+    global _raw_stream
     if stream is not None:
         return int(stream)
     import torch
-    return torch.cuda.current_stream().cuda_stream
+    if _raw_stream is None:
+        # PyTorch's raw current-stream accessor costs a fraction of building
+        # a Stream object (torch.cuda.current_stream()) on every call
+        getter = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if getter is not None:
+            _raw_stream = lambda: getter(torch._C._cuda_getDevice())
+        else:
+            _raw_stream = lambda: torch.cuda.current_stream().cuda_stream
+    return _raw_stream()
 
 
 def _ptr(t) -> int | None:
