@@ -663,8 +663,8 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
 
     // ------------------------------------------------------------- teardown
     // Lane 0 of warps 0-2 ran its role alone: reconverge each warp before the
-    // CTA barrier (bar.sync counts a warp as arrived when any of its lanes
-    // executes it, so a diverged warp would let the barrier open early).
+    // CTA barrier (bar.sync is the aligned form, which expects every thread of
+    // a warp to execute it together).
     tc_fence_before();
     __syncwarp();
     __syncthreads();
