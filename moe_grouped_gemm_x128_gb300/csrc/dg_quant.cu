@@ -6,11 +6,13 @@
 // Rule per group: amax = max|x|, s = max(amax, 1e-4f) / 448 (IEEE fp32
 // division), q = E4M3 RNE with saturation of fp32(x / s) (IEEE division).
 //
-// The activation quantiser is HBM-bound: 4 (or 2) bytes in and 1 + 4/128
-// bytes out per element.  One warp quantises one 128-value group with one
-// 16-byte load per lane; a block of 8 warps covers 8 consecutive rows x 4
-// consecutive groups so that each warp keeps 4 independent loads in flight and
-// the 8 scales of one group column land in one 32-byte sector.
+// The activation quantiser is HBM-bound on large inputs: 4 (or 2) bytes in
+// and 1 + 4/128 bytes out per element.  One warp quantises one 128-value group
+// with one 16-byte load per lane; a block of 8 warps covers 8 consecutive rows
+// x GPW consecutive groups, so that the 8 scales of one group column land in
+// one 32-byte sector.  Large inputs take GPW = 4 (four independent loads in
+// flight per warp); small ones, latency-bound, take GPW = 1 so that the
+// IEEE-division chains spread over more warps.
 #include "dg_common.h"
 #include "dg_ptx.cuh"
 
@@ -18,7 +20,6 @@ namespace dg {
 namespace {
 
 constexpr int kQuantWarps = 8;        // rows per block
-constexpr int kQuantGroupsPerWarp = 4;  // K-groups per warp
 
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
 {
@@ -53,7 +54,7 @@ __device__ __forceinline__ float4 load_group4(const uint16_t *x, size_t off)
     return f;
 }
 
-template <typename T>
+template <typename T, int GPW>
 __global__ void __launch_bounds__(kQuantWarps * 32) quant_act_1x128_kernel(const T *__restrict__ x,
                                                                           uint8_t *__restrict__ q,
                                                                           float *__restrict__ sfa, int M, int K,
@@ -61,7 +62,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quant_act_1x128_kernel(const
 {
     const int KB = K / kQBlock;
     const int row_tiles = (M + kQuantWarps - 1) / kQuantWarps;
-    const int col_tiles = (KB + kQuantGroupsPerWarp - 1) / kQuantGroupsPerWarp;
+    const int col_tiles = (KB + GPW - 1) / GPW;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // a GEMM launched after this kernel may start its prologue now; it waits
@@ -69,16 +70,16 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quant_act_1x128_kernel(const
     griddep_launch_dependents();
     for (int task = blockIdx.x; task < row_tiles * col_tiles; task += gridDim.x) {
         const int m = (task / col_tiles) * kQuantWarps + warp;
-        const int kb0 = (task % col_tiles) * kQuantGroupsPerWarp;
+        const int kb0 = (task % col_tiles) * GPW;
         if (m >= M)
             continue;
-        float4 v[kQuantGroupsPerWarp];
+        float4 v[GPW];
 #pragma unroll
-        for (int j = 0; j < kQuantGroupsPerWarp; ++j)
+        for (int j = 0; j < GPW; ++j)
             if (kb0 + j < KB)
                 v[j] = load_group4(x, static_cast<size_t>(m) * K + static_cast<size_t>(kb0 + j) * kQBlock + lane * 4);
 #pragma unroll
-        for (int j = 0; j < kQuantGroupsPerWarp; ++j) {
+        for (int j = 0; j < GPW; ++j) {
             const int kb = kb0 + j;
             if (kb >= KB)
                 break;
@@ -163,16 +164,30 @@ extern "C" dg_status_t dg_quant_act_1x128(const void *x, int x_dtype, uint8_t *q
     if (st != DG_OK)
         return st;
     const int KB = K / kQBlock;
-    const long long tasks = static_cast<long long>(ceil_div(M, kQuantWarps)) * ceil_div(KB, kQuantGroupsPerWarp);
+    // four groups per warp keep four loads in flight on large problems; a small
+    // problem (less than one full wave of such tasks) takes one group per warp,
+    // spreading the division chains over more warps
+    const long long tasks4 = static_cast<long long>(ceil_div(M, kQuantWarps)) * ceil_div(KB, 4);
+    const int gpw = tasks4 >= info.sm_count * 8LL ? 4 : 1;
+    const long long tasks = static_cast<long long>(ceil_div(M, kQuantWarps)) * ceil_div(KB, gpw);
     const int grid = static_cast<int>(tasks < info.sm_count * 8LL ? tasks : info.sm_count * 8LL);
     const int ldsfa = round_up(M, 4);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (x_dtype == DG_DTYPE_F32)
-        quant_act_1x128_kernel<float><<<grid, kQuantWarps * 32, 0, s>>>(static_cast<const float *>(x), q, sfa, M,
-                                                                         K, ldsfa);
-    else
-        quant_act_1x128_kernel<uint16_t><<<grid, kQuantWarps * 32, 0, s>>>(static_cast<const uint16_t *>(x), q,
-                                                                            sfa, M, K, ldsfa);
+    if (x_dtype == DG_DTYPE_F32) {
+        if (gpw == 4)
+            quant_act_1x128_kernel<float, 4><<<grid, kQuantWarps * 32, 0, s>>>(static_cast<const float *>(x), q, sfa,
+                                                                                M, K, ldsfa);
+        else
+            quant_act_1x128_kernel<float, 1><<<grid, kQuantWarps * 32, 0, s>>>(static_cast<const float *>(x), q, sfa,
+                                                                                M, K, ldsfa);
+    } else {
+        if (gpw == 4)
+            quant_act_1x128_kernel<uint16_t, 4><<<grid, kQuantWarps * 32, 0, s>>>(static_cast<const uint16_t *>(x), q,
+                                                                                   sfa, M, K, ldsfa);
+        else
+            quant_act_1x128_kernel<uint16_t, 1><<<grid, kQuantWarps * 32, 0, s>>>(static_cast<const uint16_t *>(x), q,
+                                                                                   sfa, M, K, ldsfa);
+    }
     return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }
 
