@@ -200,6 +200,63 @@ def grouped_masked(a, sfa, b, sfb, masked_m, d=None):
     return d
 
 
+# ------------------------------------------- GEMMs with re-quantised output --
+# The fused output (the next step after the path: the pages' call to fuse the
+# operations around a GEMM so that its result makes no extra round trip,
+# 2kiu.com tutorial 7) is the GEMM's bf16 output re-quantised as the next
+# GEMM's activation operand: E4M3 with one fp32 scale per 1x128 group of each
+# output row.  It is the plain composition of two pinned functions,
+# quant_act_1x128(bf16 D), so that it equals the unfused two-call pipeline.
+def _requant_rows(d_bits: np.ndarray, rows: np.ndarray, q: np.ndarray, sfo: np.ndarray) -> None:
+    """Quantise the listed rows of bf16 D (uint16 [M,N]) into q / sfo in place."""
+    if len(rows) == 0:
+        return
+    qr, sr = quant_act_1x128(np.ascontiguousarray(d_bits[rows]))
+    q[rows] = qr
+    sfo[:, rows] = sr[:, :len(rows)]
+
+
+def gemm_nt_quant(a, sfa, b, sfb, q=None, sfo=None):
+    """Dense D = A.B^T as gemm_nt, re-quantised: returns (q uint8 [M,N],
+    sfo fp32 [N/128, round_up(M,4)]).  N must be a multiple of 128."""
+    M = a.shape[0]
+    N = b.shape[0]
+    assert N % QBLOCK == 0
+    q = np.zeros((M, N), np.uint8) if q is None else q
+    sfo = np.zeros((N // QBLOCK, round_up(M, 4)), np.float32) if sfo is None else sfo
+    _requant_rows(gemm_nt(a, sfa, b, sfb), np.arange(M), q, sfo)
+    return q, sfo
+
+
+def grouped_contiguous_quant(a, sfa, b, sfb, m_indices, q=None, sfo=None):
+    """Contiguous layout, re-quantised.  Rows with a negative expert index keep
+    q's and sfo's contents."""
+    sum_M = a.shape[0]
+    N = b.shape[1]
+    assert N % QBLOCK == 0
+    q = np.zeros((sum_M, N), np.uint8) if q is None else q
+    sfo = np.zeros((N // QBLOCK, round_up(sum_M, 4)), np.float32) if sfo is None else sfo
+    d = grouped_contiguous(a, sfa, b, sfb, m_indices)
+    _requant_rows(d, np.flatnonzero(np.asarray(m_indices) >= 0), q, sfo)
+    return q, sfo
+
+
+def grouped_masked_quant(a, sfa, b, sfb, masked_m, q=None, sfo=None):
+    """Masked layout, re-quantised: q uint8 [G,max_m,N], sfo fp32
+    [G, N/128, round_up(max_m,4)].  Rows at or beyond masked_m[g] keep q's and
+    sfo's contents."""
+    G, max_m, _ = a.shape
+    N = b.shape[1]
+    assert N % QBLOCK == 0
+    q = np.zeros((G, max_m, N), np.uint8) if q is None else q
+    sfo = np.zeros((G, N // QBLOCK, round_up(max_m, 4)), np.float32) if sfo is None else sfo
+    d = grouped_masked(a, sfa, b, sfb, masked_m)
+    for g in range(G):
+        mm = int(min(max(int(masked_m[g]), 0), max_m))
+        _requant_rows(d[g], np.arange(mm), q[g], sfo[g])
+    return q, sfo
+
+
 def bf16_bits_to_f32(d: np.ndarray) -> np.ndarray:
     """Widen bf16 bit patterns (uint16) to fp32 exactly."""
     return (d.astype(np.uint32) << 16).view(np.float32)

@@ -14,6 +14,7 @@ import torch
 
 import oracle
 import workloads as wl
+from helpers import random_dense
 
 QB = 128
 
@@ -388,3 +389,58 @@ def test_masked_full_equals_batched_dense():
     for e in range(G):
         ref = exact_reference(ai[e], bi[e], sfa[e], sfb[e])
         np.testing.assert_array_equal(out[e], _bf16_bits(ref.astype(np.float32)))
+
+
+# ------------------------------------------------- re-quantised GEMM output --
+def _check_requant(d_bits, q, sfo, rows):
+    """Each listed row of q/sfo re-encodes the bf16 output d_bits: within the
+    quantiser's round-trip bound, and each group's largest element on +-448."""
+    dec = oracle.e4m3_decode_table()
+    d = oracle.bf16_bits_to_f32(d_bits).astype(np.float64)
+    for nb in range(d.shape[1] // QB):
+        cols = slice(nb * QB, (nb + 1) * QB)
+        s = sfo[nb, rows].astype(np.float64)[:, None]
+        x = d[rows][:, cols]
+        back = dec[q[rows][:, cols]] * s
+        assert np.all(np.abs(x - back) <= (2.0 ** -4 + 2.0 ** -20) * np.abs(x) + 2.0 ** -10 * s)
+        big = np.abs(x).max(axis=1) >= 1e-4
+        idx = np.abs(x).argmax(axis=1)
+        codes = q[rows][np.arange(len(rows)), nb * QB + idx]
+        assert np.all((codes[big] & 0x7F) == 0x7E)
+
+
+def test_gemm_quant_reencodes_the_bf16_output():
+    a, sfa, b, sfb = random_dense(130, 384, 640, seed=41)
+    q, sfo = oracle.gemm_nt_quant(a, sfa, b, sfb)
+    assert q.shape == (130, 384) and sfo.shape == (3, 132)
+    _check_requant(oracle.gemm_nt(a, sfa, b, sfb), q, sfo, np.arange(130))
+    assert np.all(sfo[:, 130:] == 0)
+
+
+def test_grouped_quant_leaves_uncomputed_rows():
+    # masked: rows at or beyond masked_m keep their contents
+    g = np.random.default_rng(5)
+    G, max_m, N, K = 3, 70, 256, 256
+    a = np.stack([random_dense(max_m, N, K, seed=50 + e)[0] for e in range(G)])
+    sfa = np.stack([random_dense(max_m, N, K, seed=50 + e)[1] for e in range(G)])
+    b = np.stack([random_dense(8, N, K, seed=60 + e)[2] for e in range(G)])
+    sfb = np.stack([random_dense(8, N, K, seed=60 + e)[3] for e in range(G)])
+    mm = np.array([70, 0, 33], np.int32)
+    q0 = g.integers(0, 256, (G, max_m, N)).astype(np.uint8)
+    s0 = g.random((G, N // QB, oracle.round_up(max_m, 4))).astype(np.float32)
+    q, sfo = oracle.grouped_masked_quant(a, sfa, b, sfb, mm, q0.copy(), s0.copy())
+    d = oracle.grouped_masked(a, sfa, b, sfb, mm)
+    for e in range(G):
+        _check_requant(d[e], q[e], sfo[e], np.arange(mm[e]))
+        np.testing.assert_array_equal(q[e, mm[e]:], q0[e, mm[e]:])
+        np.testing.assert_array_equal(sfo[e][:, mm[e]:], s0[e][:, mm[e]:])
+    # contiguous: padding rows (index -1) keep their contents
+    counts, mi, _ = wl.contiguous_routing(2, 200, seed=9)
+    ac, sac = random_dense(len(mi), N, K, seed=70)[:2]
+    q0 = g.integers(0, 256, (len(mi), N)).astype(np.uint8)
+    s0 = g.random((N // QB, oracle.round_up(len(mi), 4))).astype(np.float32)
+    q, sfo = oracle.grouped_contiguous_quant(ac, sac, b[:2], sfb[:2], mi, q0.copy(), s0.copy())
+    pad = mi < 0
+    np.testing.assert_array_equal(q[pad], q0[pad])
+    np.testing.assert_array_equal(sfo[:, :len(mi)][:, pad], s0[:, :len(mi)][:, pad])
+    _check_requant(oracle.grouped_contiguous(ac, sac, b[:2], sfb[:2], mi), q, sfo, np.flatnonzero(~pad))
