@@ -137,6 +137,32 @@ dg_status_t dg_fp8_grouped_masked(const uint8_t *a, const float *sfa, const uint
                                   const float *sfb, uint16_t *d, const int32_t *masked_m, int G,
                                   int max_m, int N, int K, int expected_m, void *stream);
 
+/* The three GEMMs above with the output re-quantised in the epilogue as the
+ * next GEMM's activation operand (2kiu.com tutorial 7: fuse the operations
+ * around a GEMM so that its result makes no extra round trip; DeepGEMM page
+ * 应用场景/混合专家模型: the expert GEMMs run back to back).  Instead of bf16 D the
+ * call writes, for every row it would have written:
+ *   q   out uint8 E4M3 codes, D's layout ([M][N], [sum_M][N], [G][max_m][N]);
+ *   sfo out fp32 one scale per 1x128 group of the row, M-major like sfa:
+ *       dense [N/128][round_up(M,4)], contiguous [N/128][sum_M],
+ *       masked [G][N/128][round_up(max_m,4)].
+ * Per row and 128-column group: D rounded to bf16 (round to nearest even),
+ * then the dg_quant_act_1x128 rule on those values, so that the result equals
+ * dg_fp8_gemm_nt (or the grouped call) followed by dg_quant_act_1x128 on D,
+ * bit for bit.  Rows not written by the bf16 call (padding, masked tails)
+ * keep their q bytes and sfo entries.  N must be a multiple of 128
+ * (DG_ERR_UNSUPPORTED_SHAPE); q and sfo 16-byte aligned (DG_ERR_MISALIGNED).
+ * The tiles are 128 x 128 whatever the plan says for the bf16 call. */
+dg_status_t dg_fp8_gemm_nt_q(const uint8_t *a, const float *sfa, const uint8_t *b, const float *sfb,
+                             uint8_t *q, float *sfo, int M, int N, int K, void *stream);
+dg_status_t dg_fp8_grouped_contiguous_q(const uint8_t *a, const float *sfa, const uint8_t *b,
+                                        const float *sfb, uint8_t *q, float *sfo,
+                                        const int32_t *m_indices, int sum_M, int N, int K, int G,
+                                        void *stream);
+dg_status_t dg_fp8_grouped_masked_q(const uint8_t *a, const float *sfa, const uint8_t *b,
+                                    const float *sfb, uint8_t *q, float *sfo, const int32_t *masked_m,
+                                    int G, int max_m, int N, int K, int expected_m, void *stream);
+
 /* Host-only: the tile plan the GEMM entry points would launch for this
  * problem on a GPU with `num_sms` SMs (num_sms <= 0: the current device's).
  * Makes no CUDA call when num_sms > 0.  For DG_LAYOUT_DENSE, M is the row

@@ -47,6 +47,9 @@ EXPORTED = (
     "dg_fp8_gemm_nt",
     "dg_fp8_grouped_contiguous",
     "dg_fp8_grouped_masked",
+    "dg_fp8_gemm_nt_q",
+    "dg_fp8_grouped_contiguous_q",
+    "dg_fp8_grouped_masked_q",
     "dg_query_plan",
     "dg_status_string",
     "dg_read_device_status",
@@ -89,6 +92,9 @@ def load() -> ctypes.CDLL:
         "dg_fp8_gemm_nt": [P, P, P, P, P, I, I, I, P],
         "dg_fp8_grouped_contiguous": [P, P, P, P, P, P, I, I, I, I, P],
         "dg_fp8_grouped_masked": [P, P, P, P, P, P, I, I, I, I, I, P],
+        "dg_fp8_gemm_nt_q": [P, P, P, P, P, P, I, I, I, P],
+        "dg_fp8_grouped_contiguous_q": [P, P, P, P, P, P, P, I, I, I, I, P],
+        "dg_fp8_grouped_masked_q": [P, P, P, P, P, P, P, I, I, I, I, I, P],
         "dg_query_plan": [I, I, I, I, I, I, ctypes.POINTER(dg_plan_t)],
         "dg_read_device_status": [ctypes.POINTER(ctypes.c_int), P],
     }
@@ -213,6 +219,53 @@ def dg_fp8_grouped_masked(a, sfa, b, sfb, masked_m, d=None, expected_m: int = 0,
            load().dg_fp8_grouped_masked(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(d), _ptr(masked_m), G, max_m,
                                         N, K, expected_m, _stream(stream)))
     return d
+
+
+# --------------------------------------------- GEMMs, re-quantised output --
+def _qout(shape, rows_ld: int, groups_shape, device, q, sfo):
+    import torch
+    if q is None:
+        q = torch.empty(shape, dtype=torch.uint8, device=device)
+    if sfo is None:
+        sfo = torch.zeros((*groups_shape, rows_ld), dtype=torch.float32, device=device)
+    assert q.is_contiguous() and sfo.is_contiguous()
+    return q, sfo
+
+
+def dg_fp8_gemm_nt_q(a, sfa, b, sfb, q=None, sfo=None, stream=None):
+    """Dense D = A . B^T re-quantised: returns (q uint8 [M, N],
+    sfo fp32 [N/128, round_up(M, 4)])."""
+    M, K = a.shape
+    N = b.shape[0]
+    q, sfo = _qout((M, N), round_up(M, 4), (N // QBLOCK,), a.device, q, sfo)
+    _check("dg_fp8_gemm_nt_q", load().dg_fp8_gemm_nt_q(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(q), _ptr(sfo),
+                                                       M, N, K, _stream(stream)))
+    return q, sfo
+
+
+def dg_fp8_grouped_contiguous_q(a, sfa, b, sfb, m_indices, q=None, sfo=None, stream=None):
+    """Contiguous MoE layout, re-quantised: returns (q uint8 [sum_M, N],
+    sfo fp32 [N/128, sum_M]); rows with index -1 are left untouched."""
+    sum_M, K = a.shape
+    G, N, _ = b.shape
+    q, sfo = _qout((sum_M, N), sum_M, (N // QBLOCK,), a.device, q, sfo)
+    _check("dg_fp8_grouped_contiguous_q",
+           load().dg_fp8_grouped_contiguous_q(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(q), _ptr(sfo),
+                                              _ptr(m_indices), sum_M, N, K, G, _stream(stream)))
+    return q, sfo
+
+
+def dg_fp8_grouped_masked_q(a, sfa, b, sfb, masked_m, q=None, sfo=None, expected_m: int = 0, stream=None):
+    """Masked MoE layout, re-quantised: returns (q uint8 [G, max_m, N],
+    sfo fp32 [G, N/128, round_up(max_m, 4)]); rows >= masked_m[g] are left
+    untouched."""
+    G, max_m, K = a.shape
+    N = b.shape[1]
+    q, sfo = _qout((G, max_m, N), round_up(max_m, 4), (G, N // QBLOCK), a.device, q, sfo)
+    _check("dg_fp8_grouped_masked_q",
+           load().dg_fp8_grouped_masked_q(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(q), _ptr(sfo),
+                                          _ptr(masked_m), G, max_m, N, K, expected_m, _stream(stream)))
+    return q, sfo
 
 
 def dg_query_plan(layout: int, M: int, N: int, K: int, G: int = 1, num_sms: int = 0) -> dict:

@@ -88,11 +88,14 @@ struct SmemLayout {
     static constexpr int kOutWarpBytes = 32 * kOutRowStride;
     static constexpr int kOutOff = kBOff + STAGES * kBBytes;
     static constexpr int kBarOff = kOutOff + (BN / EPI_COLS) * 4 * kOutWarpBytes;
-    // full[S], empty[S], tfull[kMaxBufs], tempty[kMaxBufs], drain[2]
-    static constexpr int kNumBars = 2 * STAGES + 2 * kMaxBufs + 2;
+    // full[S], empty[S], tfull[kMaxBufs], tempty[kMaxBufs], drain[2], xchg[4]
+    static constexpr int kNumBars = 2 * STAGES + 2 * kMaxBufs + 2 + 4;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;   // tmem base, abort flag
     static constexpr int kPrefixOff = kMiscOff + 16;
-    static constexpr int kBytes = kPrefixOff + (kMaxMaskedGroups + 1) * 4;
+    // re-quantised output: per-row amax halves exchanged between the two
+    // warpgroups of a 128-column group, double-buffered by tile parity
+    static constexpr int kAmaxOff = kPrefixOff + (kMaxMaskedGroups + 1) * 4;
+    static constexpr int kBytes = kAmaxOff + 2 * 2 * kBM * 4;
     static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1024
 };
 
@@ -215,14 +218,21 @@ struct Sched {
     }
 };
 
-template <int BN, int STAGES, int EPI_COLS, int KPS>
+// QOUT: instead of bf16 D, write D re-quantised as the next GEMM's activation
+// operand: E4M3 codes qout (D's layout, one byte per element) and one fp32
+// scale per 1x128 group of each row, sfo [(G,) N/128][ldsfa] (M-major), each
+// group's scale and codes computed from the bf16-rounded values exactly as
+// the 1x128 quantiser does.  Needs 128-column groups inside one tile (BN =
+// 128, two 64-column warpgroups).
+template <int BN, int STAGES, int EPI_COLS, int KPS, bool QOUT>
 __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const float *__restrict__ sfa, const float *__restrict__ sfb,
-                    uint16_t *__restrict__ d, const int32_t *__restrict__ meta, Problem p,
-                    unsigned int *status)
+                    uint16_t *__restrict__ d, uint8_t *__restrict__ qout, float *__restrict__ sfo,
+                    const int32_t *__restrict__ meta, Problem p, unsigned int *status)
 {
     using L = SmemLayout<BN, STAGES, EPI_COLS, KPS>;
+    static_assert(!QOUT || (BN == 128 && EPI_COLS == 64), "re-quantised output needs one 128-column group per tile");
     constexpr int kNumEpiWarps = Roles<BN, EPI_COLS>::kNumEpiWarps;
     // TMEM slots: one per ring stage in flight between the MMAs and the
     // epilogue, each holding the KPS partial products (128 x BN fp32) of one
@@ -261,6 +271,8 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + kMaxBufs + b); };
     auto drain_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 2 * kMaxBufs + i); };
+    // re-quantised output: the two warps holding rows 32q..32q+31 meet here
+    auto xchg_bar = [&](int q) { return bar0 + 8u * (2 * STAGES + 2 * kMaxBufs + 2 + q); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::kMiscOff + 4);
     int *prefix = reinterpret_cast<int *>(smem + L::kPrefixOff);
@@ -283,6 +295,9 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
         }
         for (int i = 0; i < kIssuers; ++i)
             mbar_init(drain_bar(i), 1);
+        if constexpr (QOUT)
+            for (int i = 0; i < 4; ++i)
+                mbar_init(xchg_bar(i), 64);
         *abort_flag = 0;
         fence_mbarrier_init();
         fence_proxy_async_smem();
@@ -496,6 +511,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
         int buf = 0;
         uint32_t tph = 0;
         bool ok = true;
+        uint32_t tile_par = 0;   // alternates per tile done (QOUT's amax exchange buffer)
         for (int t = blockIdx.x; ok && t < sch.num_tiles; t += gridDim.x) {
             const TileInfo ti = sch.tile(t, p, meta);
             if (ti.skip) {
@@ -632,7 +648,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
             // then the warp writes 32 rows x kCols out row-major, so that one
             // instruction covers whole row segments.  Rows that must not be
             // written (edges, masked tails, padding) are skipped.
-            {
+            if constexpr (!QOUT) {
                 uint8_t *const stage = smem + L::kOutOff + (warp - kEpiWarp0) * L::kOutWarpBytes;
                 const uint32_t my_row = smem_u32(stage) + lane * L::kOutRowStride;
 #pragma unroll
@@ -657,6 +673,72 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
                     }
                 }
                 __syncwarp();
+            } else {
+                // Re-quantised output.  The two warpgroups hold the two 64-column
+                // halves of each row's 128-column group: each rounds its values
+                // to bf16, and the row's amax is the larger of the two halves'.
+                float m = 0.0f;
+#pragma unroll
+                for (int j = 0; j < kCols / 2; ++j) {
+                    const uint32_t pk = pack_bf16x2(acc[j].x, acc[j].y);
+                    acc[j] = make_float2(__uint_as_float(pk << 16), __uint_as_float(pk & 0xFFFF0000u));
+                    m = fmaxf(m, fmaxf(fabsf(acc[j].x), fabsf(acc[j].y)));
+                }
+                float *const amax_x = reinterpret_cast<float *>(smem + L::kAmaxOff) + tile_par * 2 * kBM;
+                amax_x[grp * kBM + r] = m;
+                // the two warps holding these 32 rows meet at xchg_bar(q), one
+                // phase per tile, with a bounded wait (a partner that gave up
+                // on an earlier wait never arrives)
+                mbar_arrive(xchg_bar(q));
+                uint32_t met = 1;
+                if (lane == 0)
+                    met = wait_phase(xchg_bar(q), tile_par, abort_flag, status) ? 1u : 0u;
+                if (__shfl_sync(0xffffffffu, met, 0) == 0) {
+                    ok = false;
+                    break;
+                }
+                __syncwarp();
+                const float amax = fmaxf(m, amax_x[(grp ^ 1) * kBM + r]);
+                const float sc = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
+                uint8_t *const stage = smem + L::kOutOff + (warp - kEpiWarp0) * L::kOutWarpBytes;
+                const uint32_t my_row = smem_u32(stage) + lane * L::kOutRowStride;
+#pragma unroll
+                for (int c = 0; c < kCols / 16; ++c) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float2 lo = acc[c * 8 + 2 * u];
+                        const float2 hi = acc[c * 8 + 2 * u + 1];
+                        w4[u] = e4m3x4(__fdiv_rn(lo.x, sc), __fdiv_rn(lo.y, sc), __fdiv_rn(hi.x, sc),
+                                       __fdiv_rn(hi.y, sc));
+                    }
+                    st_shared_v4(my_row + c * 16, w4[0], w4[1], w4[2], w4[3]);
+                }
+                __syncwarp();
+                const uint32_t rows_ok = __ballot_sync(0xffffffffu, row_ok);
+                const size_t warp_row0 = d_row - lane;
+                constexpr int kChunksPerRow = kCols / 16;        // 16-byte chunks of codes per row
+#pragma unroll
+                for (int i = 0; i < kChunksPerRow; ++i) {
+                    const int idx = i * 32 + lane;
+                    const int rr = idx / kChunksPerRow;
+                    const int cc = idx % kChunksPerRow;
+                    const int col = ti.n0 + c0 + cc * 16;
+                    if (((rows_ok >> rr) & 1u) && col < p.N) {
+                        const uint4 v = ld_shared_v4(smem_u32(stage) + rr * L::kOutRowStride + cc * 16);
+                        st_global_v4(qout + (warp_row0 + rr) * p.N + col, v.x, v.y, v.z, v.w);
+                    }
+                }
+                if (grp == 0 && row_ok) {
+                    // scales M-major: [(g,) n-group][row], the activation layout
+                    const size_t ngroups = static_cast<size_t>(p.N) / 128;
+                    const size_t srow = p.layout == DG_LAYOUT_MASKED ? static_cast<size_t>(ti.m0 + r) : d_row;
+                    const size_t sgrp = (p.layout == DG_LAYOUT_MASKED ? static_cast<size_t>(ti.g) * ngroups : 0) +
+                                        static_cast<size_t>(ti.n0 / 128);
+                    sfo[sgrp * p.ldsfa + srow] = sc;
+                }
+                __syncwarp();
+                tile_par ^= 1u;
             }
         }
     }
@@ -720,12 +802,13 @@ int smem_for(int bn)
                       : SmemLayout<128, kCfg128.stages, kCfg128.epi_cols, kCfg128.kps>::kAlloc;
 }
 
-Plan make_plan(int layout, int M, int N, int K, int G, int num_sms)
+Plan make_plan(int layout, int M, int N, int K, int G, int num_sms, bool qout = false)
 {
     (void)K;
     Plan pl;
     const int mblk = layout == DG_LAYOUT_MASKED ? G * ceil_div(M, kBM) : ceil_div(M, kBM);
-    int bn = forced_bn();
+    // a re-quantised output needs each 128-column scale group inside one tile
+    int bn = qout ? 128 : forced_bn();
     if (bn == 0) {
         if (static_cast<long long>(mblk) * ceil_div(N, 192) >= num_sms) {
             bn = 192;
@@ -768,13 +851,14 @@ dg_status_t check_common(const void *a, const void *sfa, const void *b, const vo
 }
 
 dg_status_t launch(int layout, const uint8_t *a, const float *sfa, const uint8_t *b, const float *sfb, uint16_t *d,
-                   const int32_t *meta, int M, int N, int K, int G, void *stream)
+                   uint8_t *qout, float *sfo, const int32_t *meta, int M, int N, int K, int G, void *stream)
 {
     DeviceInfo info;
     dg_status_t st = current_device(&info);
     if (st != DG_OK)
         return st;
-    const Plan pl = make_plan(layout, M, N, K, G, info.sm_count);
+    const bool qmode = qout != nullptr;
+    const Plan pl = make_plan(layout, M, N, K, G, info.sm_count, qmode);
     const int ldsfa = round_up(M, 4);
 
     // Tensor maps view each K-major operand as [..][rows][K/128][128 bytes]:
@@ -806,9 +890,10 @@ dg_status_t launch(int layout, const uint8_t *a, const float *sfa, const uint8_t
         if (st != DG_OK)
             return st;
     }
-    auto kernel = pl.bn == 192  ? fp8_gemm_kernel<192, kCfg192.stages, kCfg192.epi_cols, kCfg192.kps>
-                  : pl.bn == 96 ? fp8_gemm_kernel<96, kCfg96.stages, kCfg96.epi_cols, kCfg96.kps>
-                                : fp8_gemm_kernel<128, kCfg128.stages, kCfg128.epi_cols, kCfg128.kps>;
+    auto kernel = qmode         ? fp8_gemm_kernel<128, kCfg128.stages, kCfg128.epi_cols, kCfg128.kps, true>
+                  : pl.bn == 192 ? fp8_gemm_kernel<192, kCfg192.stages, kCfg192.epi_cols, kCfg192.kps, false>
+                  : pl.bn == 96  ? fp8_gemm_kernel<96, kCfg96.stages, kCfg96.epi_cols, kCfg96.kps, false>
+                                 : fp8_gemm_kernel<128, kCfg128.stages, kCfg128.epi_cols, kCfg128.kps, false>;
     const int threads = pl.bn == 192  ? Roles<192, kCfg192.epi_cols>::kThreads
                         : pl.bn == 96 ? Roles<96, kCfg96.epi_cols>::kThreads
                                       : Roles<128, kCfg128.epi_cols>::kThreads;
@@ -826,7 +911,7 @@ dg_status_t launch(int layout, const uint8_t *a, const float *sfa, const uint8_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, sfa, sfb, d, meta, prob, info.status_word) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, sfa, sfb, d, qout, sfo, meta, prob, info.status_word) != cudaSuccess)
         return DG_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }
@@ -840,7 +925,7 @@ extern "C" dg_status_t dg_fp8_gemm_nt(const uint8_t *a, const float *sfa, const 
     dg_status_t st = dg::check_common(a, sfa, b, sfb, d, M, N, K);
     if (st != DG_OK)
         return st;
-    return dg::launch(DG_LAYOUT_DENSE, a, sfa, b, sfb, d, nullptr, M, N, K, 1, stream);
+    return dg::launch(DG_LAYOUT_DENSE, a, sfa, b, sfb, d, nullptr, nullptr, nullptr, M, N, K, 1, stream);
 }
 
 extern "C" dg_status_t dg_fp8_grouped_contiguous(const uint8_t *a, const float *sfa, const uint8_t *b,
@@ -856,7 +941,7 @@ extern "C" dg_status_t dg_fp8_grouped_contiguous(const uint8_t *a, const float *
         return DG_ERR_UNSUPPORTED_SHAPE;
     if (!dg::aligned16(m_indices))
         return DG_ERR_MISALIGNED;
-    return dg::launch(DG_LAYOUT_CONTIGUOUS, a, sfa, b, sfb, d, m_indices, sum_M, N, K, G, stream);
+    return dg::launch(DG_LAYOUT_CONTIGUOUS, a, sfa, b, sfb, d, nullptr, nullptr, m_indices, sum_M, N, K, G, stream);
 }
 
 extern "C" dg_status_t dg_fp8_grouped_masked(const uint8_t *a, const float *sfa, const uint8_t *b,
@@ -873,7 +958,73 @@ extern "C" dg_status_t dg_fp8_grouped_masked(const uint8_t *a, const float *sfa,
         return DG_ERR_UNSUPPORTED_SHAPE;
     if (!dg::aligned16(masked_m))
         return DG_ERR_MISALIGNED;
-    return dg::launch(DG_LAYOUT_MASKED, a, sfa, b, sfb, d, masked_m, max_m, N, K, G, stream);
+    return dg::launch(DG_LAYOUT_MASKED, a, sfa, b, sfb, d, nullptr, nullptr, masked_m, max_m, N, K, G, stream);
+}
+
+// ---------------------------------------- re-quantised output (E4M3 + 1x128)
+namespace dg {
+namespace {
+dg_status_t check_qout(const uint8_t *q, const float *sfo, int N)
+{
+    if (!q || !sfo)
+        return DG_ERR_INVALID_ARG;
+    if (N % 128 != 0)
+        return DG_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(q) || !aligned16(sfo))
+        return DG_ERR_MISALIGNED;
+    return DG_OK;
+}
+}  // namespace
+}  // namespace dg
+
+extern "C" dg_status_t dg_fp8_gemm_nt_q(const uint8_t *a, const float *sfa, const uint8_t *b, const float *sfb,
+                                        uint8_t *q, float *sfo, int M, int N, int K, void *stream)
+{
+    // the D check of check_common is made on q (its address and alignment)
+    dg_status_t st = dg::check_common(a, sfa, b, sfb, q, M, N, K);
+    if (st == DG_OK)
+        st = dg::check_qout(q, sfo, N);
+    if (st != DG_OK)
+        return st;
+    return dg::launch(DG_LAYOUT_DENSE, a, sfa, b, sfb, nullptr, q, sfo, nullptr, M, N, K, 1, stream);
+}
+
+extern "C" dg_status_t dg_fp8_grouped_contiguous_q(const uint8_t *a, const float *sfa, const uint8_t *b,
+                                                   const float *sfb, uint8_t *q, float *sfo,
+                                                   const int32_t *m_indices, int sum_M, int N, int K, int G,
+                                                   void *stream)
+{
+    dg_status_t st = dg::check_common(a, sfa, b, sfb, q, sum_M, N, K);
+    if (st == DG_OK)
+        st = dg::check_qout(q, sfo, N);
+    if (st != DG_OK)
+        return st;
+    if (!m_indices || G <= 0)
+        return DG_ERR_INVALID_ARG;
+    if (sum_M % dg::kBM != 0)
+        return DG_ERR_UNSUPPORTED_SHAPE;
+    if (!dg::aligned16(m_indices))
+        return DG_ERR_MISALIGNED;
+    return dg::launch(DG_LAYOUT_CONTIGUOUS, a, sfa, b, sfb, nullptr, q, sfo, m_indices, sum_M, N, K, G, stream);
+}
+
+extern "C" dg_status_t dg_fp8_grouped_masked_q(const uint8_t *a, const float *sfa, const uint8_t *b,
+                                               const float *sfb, uint8_t *q, float *sfo, const int32_t *masked_m,
+                                               int G, int max_m, int N, int K, int expected_m, void *stream)
+{
+    (void)expected_m;
+    dg_status_t st = dg::check_common(a, sfa, b, sfb, q, max_m, N, K);
+    if (st == DG_OK)
+        st = dg::check_qout(q, sfo, N);
+    if (st != DG_OK)
+        return st;
+    if (!masked_m || G <= 0)
+        return DG_ERR_INVALID_ARG;
+    if (G > dg::kMaxMaskedGroups)
+        return DG_ERR_UNSUPPORTED_SHAPE;
+    if (!dg::aligned16(masked_m))
+        return DG_ERR_MISALIGNED;
+    return dg::launch(DG_LAYOUT_MASKED, a, sfa, b, sfb, nullptr, q, sfo, masked_m, max_m, N, K, G, stream);
 }
 
 extern "C" dg_status_t dg_query_plan(int layout, int M, int N, int K, int G, int num_sms, dg_plan_t *out)

@@ -322,6 +322,17 @@ __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, b
 }
 
 // ------------------------------------------------------------- epilogue ---
+// Four values to E4M3 (round to nearest even, saturating to +-448), packed
+// in order from the least significant byte.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
+{
+    uint16_t lo, hi;
+    // the first source lands in the upper byte of each pair
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     uint32_t r;

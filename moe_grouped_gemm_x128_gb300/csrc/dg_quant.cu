@@ -21,15 +21,6 @@ namespace {
 
 constexpr int kQuantWarps = 8;        // rows per block
 
-__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
-{
-    uint16_t lo, hi;
-    // the first source lands in the upper byte of each pair
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
-    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-}
-
 __device__ __forceinline__ float warp_max(float v)
 {
 #pragma unroll

@@ -79,6 +79,28 @@ def test_gemm_validation(lib):
     assert call(lib, "dg_fp8_grouped_masked", F, F, F, F, F, F, 4, 0, 256, 512, 0, None) == dg.DG_ERR_INVALID_ARG
 
 
+def test_requant_gemm_validation(lib):
+    F = FAKE
+    # q and sfo must both be given, N a multiple of 128, both 16-byte aligned
+    assert call(lib, "dg_fp8_gemm_nt_q", F, F, F, F, F, None, 128, 256, 512, None) == dg.DG_ERR_INVALID_ARG
+    assert call(lib, "dg_fp8_gemm_nt_q", F, F, F, F, None, F, 128, 256, 512, None) == dg.DG_ERR_INVALID_ARG
+    assert call(lib, "dg_fp8_gemm_nt_q", F, F, F, F, F, F, 128, 192, 512, None) == dg.DG_ERR_UNSUPPORTED_SHAPE
+    assert call(lib, "dg_fp8_gemm_nt_q", F, F, F, F, F, F + 4, 128, 256, 512, None) == dg.DG_ERR_MISALIGNED
+    assert call(lib, "dg_fp8_gemm_nt_q", F, F, F, F, F + 8, F, 128, 256, 512, None) == dg.DG_ERR_MISALIGNED
+    assert call(lib, "dg_fp8_grouped_contiguous_q", F, F, F, F, F, F, F, 200, 256, 512, 2, None) == \
+        dg.DG_ERR_UNSUPPORTED_SHAPE
+    assert call(lib, "dg_fp8_grouped_contiguous_q", F, F, F, F, F, F, None, 256, 256, 512, 2, None) == \
+        dg.DG_ERR_INVALID_ARG
+    assert call(lib, "dg_fp8_grouped_contiguous_q", F, F, F, F, F, F, F, 256, 320, 512, 2, None) == \
+        dg.DG_ERR_UNSUPPORTED_SHAPE
+    assert call(lib, "dg_fp8_grouped_masked_q", F, F, F, F, F, F, F, 5000, 256, 256, 512, 0, None) == \
+        dg.DG_ERR_UNSUPPORTED_SHAPE
+    assert call(lib, "dg_fp8_grouped_masked_q", F, F, F, F, F, F, F + 4, 4, 256, 256, 512, 0, None) == \
+        dg.DG_ERR_MISALIGNED
+    assert call(lib, "dg_fp8_grouped_masked_q", F, F, F, F, F, F, F, 4, 256, 384 + 64, 512, 0, None) == \
+        dg.DG_ERR_UNSUPPORTED_SHAPE
+
+
 def test_read_status_validation(lib):
     assert lib.dg_read_device_status(None, None) == dg.DG_ERR_INVALID_ARG
 
