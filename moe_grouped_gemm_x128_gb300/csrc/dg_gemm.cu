@@ -218,6 +218,30 @@ struct Sched {
     }
 };
 
+// v / s rounded to nearest fp32 (what IEEE division gives), for two values,
+// from y = RN(1/s) without a division per value.  q = RN(v*y) is within two
+// ulps of v/s; one remainder correction q <- RN(q + RN(v - s*q)*y) makes it
+// faithful (within one ulp), and a second one, now with an exact remainder,
+// makes it the correctly rounded quotient: Markstein's theorem for a faithful
+// quotient and a correctly rounded reciprocal (P. Markstein, IBM J. Res. Dev.
+// 34(1), 1990; J.-M. Muller et al., Handbook of Floating-Point Arithmetic,
+// division with a fused multiply-add).  The theorem needs v/s in the normal
+// range; smaller quotients become +-0 in E4M3 whatever their low bits.  The
+// sign is v's, so that -0 / s stays -0.
+__device__ __forceinline__ float2 div2_rn(float2 v, float s, float y)
+{
+    const float2 y2 = make_float2(y, y);
+    const float2 ns2 = make_float2(-s, -s);
+    float2 q = fmul2(v, y2);
+    float2 r = ffma2(q, ns2, v);
+    q = ffma2(r, y2, q);
+    r = ffma2(q, ns2, v);
+    q = ffma2(r, y2, q);
+    q.x = __uint_as_float(__float_as_uint(q.x) | (__float_as_uint(v.x) & 0x80000000u));
+    q.y = __uint_as_float(__float_as_uint(q.y) | (__float_as_uint(v.y) & 0x80000000u));
+    return q;
+}
+
 // QOUT: instead of bf16 D, write D re-quantised as the next GEMM's activation
 // operand: E4M3 codes qout (D's layout, one byte per element) and one fp32
 // scale per 1x128 group of each row, sfo [(G,) N/128][ldsfa] (M-major), each
@@ -674,15 +698,27 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
                 }
                 __syncwarp();
             } else {
-                // Re-quantised output.  The two warpgroups hold the two 64-column
-                // halves of each row's 128-column group: each rounds its values
-                // to bf16, and the row's amax is the larger of the two halves'.
+                // Re-quantised output.  Each thread rounds its 64 values to
+                // bf16, stages them in its row of the warp's shared-memory
+                // rows (128 bytes) and takes their amax; the two warpgroups
+                // hold the two 64-column halves of each row's 128-column
+                // group, and the row's amax is the larger of the halves'.
+                auto unpack = [](uint32_t w) {
+                    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+                };
+                uint8_t *const stage = smem + L::kOutOff + (warp - kEpiWarp0) * L::kOutWarpBytes;
+                const uint32_t my_row = smem_u32(stage) + lane * L::kOutRowStride;
                 float m = 0.0f;
 #pragma unroll
-                for (int j = 0; j < kCols / 2; ++j) {
-                    const uint32_t pk = pack_bf16x2(acc[j].x, acc[j].y);
-                    acc[j] = make_float2(__uint_as_float(pk << 16), __uint_as_float(pk & 0xFFFF0000u));
-                    m = fmaxf(m, fmaxf(fabsf(acc[j].x), fabsf(acc[j].y)));
+                for (int c = 0; c < kCols / 8; ++c) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        w[k] = pack_bf16x2(acc[c * 4 + k].x, acc[c * 4 + k].y);
+                        const float2 v = unpack(w[k]);
+                        m = fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y)));
+                    }
+                    st_shared_v4(my_row + c * 16, w[0], w[1], w[2], w[3]);
                 }
                 float *const amax_x = reinterpret_cast<float *>(smem + L::kAmaxOff) + tile_par * 2 * kBM;
                 amax_x[grp * kBM + r] = m;
@@ -700,19 +736,17 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
                 __syncwarp();
                 const float amax = fmaxf(m, amax_x[(grp ^ 1) * kBM + r]);
                 const float sc = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
-                uint8_t *const stage = smem + L::kOutOff + (warp - kEpiWarp0) * L::kOutWarpBytes;
-                const uint32_t my_row = smem_u32(stage) + lane * L::kOutRowStride;
-#pragma unroll
-                for (int c = 0; c < kCols / 16; ++c) {
-                    uint32_t w4[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float2 lo = acc[c * 8 + 2 * u];
-                        const float2 hi = acc[c * 8 + 2 * u + 1];
-                        w4[u] = e4m3x4(__fdiv_rn(lo.x, sc), __fdiv_rn(lo.y, sc), __fdiv_rn(hi.x, sc),
-                                       __fdiv_rn(hi.y, sc));
-                    }
-                    st_shared_v4(my_row + c * 16, w4[0], w4[1], w4[2], w4[3]);
+                const float rsc = __frcp_rn(sc);
+                // 8 values (16 bytes of bf16) in, 8 codes out, written over
+                // the front of the same row (behind what has been read)
+#pragma unroll 2
+                for (int c = 0; c < kCols / 8; ++c) {
+                    const uint4 w = ld_shared_v4(my_row + c * 16);
+                    const float2 v0 = div2_rn(unpack(w.x), sc, rsc);
+                    const float2 v1 = div2_rn(unpack(w.y), sc, rsc);
+                    const float2 v2 = div2_rn(unpack(w.z), sc, rsc);
+                    const float2 v3 = div2_rn(unpack(w.w), sc, rsc);
+                    st_shared_v2(my_row + c * 8, e4m3x4(v0.x, v0.y, v1.x, v1.y), e4m3x4(v2.x, v2.y, v3.x, v3.y));
                 }
                 __syncwarp();
                 const uint32_t rows_ok = __ballot_sync(0xffffffffu, row_ok);
