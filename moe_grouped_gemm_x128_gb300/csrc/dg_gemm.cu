@@ -218,30 +218,6 @@ struct Sched {
     }
 };
 
-// v / s rounded to nearest fp32 (what IEEE division gives), for two values,
-// from y = RN(1/s) without a division per value.  q = RN(v*y) is within two
-// ulps of v/s; one remainder correction q <- RN(q + RN(v - s*q)*y) makes it
-// faithful (within one ulp), and a second one, now with an exact remainder,
-// makes it the correctly rounded quotient: Markstein's theorem for a faithful
-// quotient and a correctly rounded reciprocal (P. Markstein, IBM J. Res. Dev.
-// 34(1), 1990; J.-M. Muller et al., Handbook of Floating-Point Arithmetic,
-// division with a fused multiply-add).  The theorem needs v/s in the normal
-// range; smaller quotients become +-0 in E4M3 whatever their low bits.  The
-// sign is v's, so that -0 / s stays -0.
-__device__ __forceinline__ float2 div2_rn(float2 v, float s, float y)
-{
-    const float2 y2 = make_float2(y, y);
-    const float2 ns2 = make_float2(-s, -s);
-    float2 q = fmul2(v, y2);
-    float2 r = ffma2(q, ns2, v);
-    q = ffma2(r, y2, q);
-    r = ffma2(q, ns2, v);
-    q = ffma2(r, y2, q);
-    q.x = __uint_as_float(__float_as_uint(q.x) | (__float_as_uint(v.x) & 0x80000000u));
-    q.y = __uint_as_float(__float_as_uint(q.y) | (__float_as_uint(v.y) & 0x80000000u));
-    return q;
-}
-
 // QOUT: instead of bf16 D, write D re-quantised as the next GEMM's activation
 // operand: E4M3 codes qout (D's layout, one byte per element) and one fp32
 // scale per 1x128 group of each row, sfo [(G,) N/128][ldsfa] (M-major), each

@@ -316,6 +316,38 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b)
     return d;
 }
 
+// v / s rounded to nearest fp32 (what IEEE division gives), for two values,
+// from y = RN(1/s) without a division per value.  q = RN(v*y) is within two
+// ulps of v/s; one remainder correction q <- RN(q + RN(v - s*q)*y) makes it
+// faithful (within one ulp), and a second one, now with an exact remainder,
+// makes it the correctly rounded quotient: Markstein's theorem for a faithful
+// quotient and a correctly rounded reciprocal (P. Markstein, IBM J. Res. Dev.
+// 34(1), 1990; J.-M. Muller et al., Handbook of Floating-Point Arithmetic,
+// division with a fused multiply-add).  The theorem needs v/s in the normal
+// range; smaller quotients become +-0 in E4M3 whatever their low bits.  The
+// sign is v's, so that -0 / s stays -0.
+__device__ __forceinline__ float2 div2_rn(float2 v, float s, float y)
+{
+    const float2 y2 = make_float2(y, y);
+    const float2 ns2 = make_float2(-s, -s);
+    float2 q = fmul2(v, y2);
+    float2 r = ffma2(q, ns2, v);
+    q = ffma2(r, y2, q);
+    r = ffma2(q, ns2, v);
+    q = ffma2(r, y2, q);
+    q.x = __uint_as_float(__float_as_uint(q.x) | (__float_as_uint(v.x) & 0x80000000u));
+    q.y = __uint_as_float(__float_as_uint(q.y) | (__float_as_uint(v.y) & 0x80000000u));
+    return q;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
 // Named barrier `id` over `count` threads that also ANDs a predicate across
 // them (bar.red.and.pred): every participant gets the same answer.
 __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, bool v)

@@ -4,7 +4,9 @@
 // saturation of out-of-range values).
 //
 // Rule per group: amax = max|x|, s = max(amax, 1e-4f) / 448 (IEEE fp32
-// division), q = E4M3 RNE with saturation of fp32(x / s) (IEEE division).
+// division), q = E4M3 RNE with saturation of fp32(x / s), the quotient
+// rounded to nearest as IEEE division rounds it (computed by div2_rn: a
+// correctly rounded reciprocal and two remainder corrections per value).
 //
 // The activation quantiser is HBM-bound on large inputs: 4 (or 2) bytes in
 // and 1 + 4/128 bytes out per element.  One warp quantises one 128-value group
@@ -12,7 +14,7 @@
 // x GPW consecutive groups, so that the 8 scales of one group column land in
 // one 32-byte sector.  Large inputs take GPW = 4 (four independent loads in
 // flight per warp); small ones, latency-bound, take GPW = 1 so that the
-// IEEE-division chains spread over more warps.
+// division chains spread over more warps.
 #include "dg_common.h"
 #include "dg_ptx.cuh"
 
@@ -20,14 +22,6 @@ namespace dg {
 namespace {
 
 constexpr int kQuantWarps = 8;        // rows per block
-
-__device__ __forceinline__ float warp_max(float v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
 
 __device__ __forceinline__ float4 load_group4(const float *x, size_t off)
 {
@@ -77,8 +71,10 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quant_act_1x128_kernel(const
             float amax = fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w)));
             amax = warp_max(amax);
             const float s = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
-            const uint32_t packed = e4m3x4(__fdiv_rn(v[j].x, s), __fdiv_rn(v[j].y, s), __fdiv_rn(v[j].z, s),
-                                           __fdiv_rn(v[j].w, s));
+            const float y = __frcp_rn(s);
+            const float2 lo = div2_rn(make_float2(v[j].x, v[j].y), s, y);
+            const float2 hi = div2_rn(make_float2(v[j].z, v[j].w), s, y);
+            const uint32_t packed = e4m3x4(lo.x, lo.y, hi.x, hi.y);
             __stcs(reinterpret_cast<uint32_t *>(q + static_cast<size_t>(m) * K + static_cast<size_t>(kb) * kQBlock) +
                        lane,
                    packed);
@@ -124,14 +120,17 @@ __global__ void __launch_bounds__(256) quant_weight_128x128_kernel(const float *
     for (int i = 1; i < 8; ++i)
         amax = fmaxf(amax, red[i]);
     const float s = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
+    const float y = __frcp_rn(s);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const int e = i * 256 + threadIdx.x;
         const int n = nb * kQBlock + e / 32;
         const int k = kb * kQBlock + (e % 32) * 4;
-        if (n < N)
-            *reinterpret_cast<uint32_t *>(qg + static_cast<size_t>(n) * K + k) =
-                e4m3x4(__fdiv_rn(v[i].x, s), __fdiv_rn(v[i].y, s), __fdiv_rn(v[i].z, s), __fdiv_rn(v[i].w, s));
+        if (n < N) {
+            const float2 lo = div2_rn(make_float2(v[i].x, v[i].y), s, y);
+            const float2 hi = div2_rn(make_float2(v[i].z, v[i].w), s, y);
+            *reinterpret_cast<uint32_t *>(qg + static_cast<size_t>(n) * K + k) = e4m3x4(lo.x, lo.y, hi.x, hi.y);
+        }
     }
     if (threadIdx.x == 0)
         sfb[(static_cast<size_t>(g) * NB + nb) * KB + kb] = s;
