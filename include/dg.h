@@ -40,6 +40,14 @@
  *     only the GPU can see: bad MoE metadata and pipeline timeouts.
  *   - Thread safety: entry points may be called concurrently from several
  *     host threads; per-device setup happens once behind a lock.
+ *   - Stream order: the kernels let the next kernel of the stream start its
+ *     set-up early (programmatic dependent launch) and wait for the previous
+ *     kernel to complete before reading its outputs, with one exception: a
+ *     dense GEMM copies the first K blocks of B before that wait.  B (the
+ *     weights) must therefore not be written by the kernel immediately before
+ *     the call in the same stream if that kernel signals its dependents early
+ *     (the activation quantiser and the GEMMs of this library do; kernels that
+ *     do not use programmatic launch never let the GEMM start early).
  */
 #ifndef DG_H_
 #define DG_H_

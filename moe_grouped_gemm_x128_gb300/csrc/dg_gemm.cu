@@ -218,6 +218,17 @@ struct Sched {
     }
 };
 
+// Register cap per thread: at 128 x 96 (the small-M tile) 112, without
+// spills, so that a CTA (512 threads) leaves 8k registers of the SM free:
+// room for one block of the activation quantiser (8 warps x 32 registers),
+// so that the GEMM launched behind it starts on an SM where one block is
+// still running.  The other tiles take what their launch bounds allow.
+template <int BN>
+constexpr int max_regs()
+{
+    return BN == 96 ? 112 : 168;
+}
+
 // QOUT: instead of bf16 D, write D re-quantised as the next GEMM's activation
 // operand: E4M3 codes qout (D's layout, one byte per element) and one fp32
 // scale per 1x128 group of each row, sfo [(G,) N/128][ldsfa] (M-major), each
@@ -225,7 +236,7 @@ struct Sched {
 // the 1x128 quantiser does.  Needs 128-column groups inside one tile (BN =
 // 128, two 64-column warpgroups).
 template <int BN, int STAGES, int EPI_COLS, int KPS, bool QOUT>
-__global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
+__global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1) __maxnreg__(max_regs<BN>())
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const float *__restrict__ sfa, const float *__restrict__ sfb,
                     uint16_t *__restrict__ d, uint8_t *__restrict__ qout, float *__restrict__ sfo,
@@ -309,9 +320,6 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
-    // the previous kernel in the stream may still be running until here
-    griddep_wait();
-
     Sched<BN> sch;
     sch.n_blocks = (p.N + BN - 1) / BN;
     sch.G = p.G;
@@ -349,22 +357,31 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
             p_t += gridDim.x;
         }
     };
+    // dense: stages of the first tile whose B copy (with the stage's
+    // expect-tx) went out before the previous kernel had finished; only
+    // their A copy is left to issue
+    int p_pre = 0;
     // issues the loads of the unit under the cursor into the current stage
     auto p_issue = [&]() {
         const uint32_t fb = full_bar(p_stage);
-        mbar_arrive_expect_tx(fb, kStageTx);
         const uint32_t a_dst = sbase + L::kAOff + p_stage * L::kABytes;
         const uint32_t b_dst = sbase + L::kBOff + p_stage * L::kBBytes;
         // tensor maps view K as (128 bytes) x (K blocks); a box covers KPS
         // K blocks (past the last one it is zero-filled)
         const int kb0 = p_u * KPS;
-        if (p.layout == DG_LAYOUT_DENSE) {
+        if (p_pre > 0) {
+            --p_pre;
+            tma_load_3d(a_dst, &tmap_a, fb, 0, p_ti.m0, kb0);
+        } else if (p.layout == DG_LAYOUT_DENSE) {
+            mbar_arrive_expect_tx(fb, kStageTx);
             tma_load_3d(a_dst, &tmap_a, fb, 0, p_ti.m0, kb0);
             tma_load_3d(b_dst, &tmap_b, fb, 0, p_ti.n0, kb0);
         } else if (p.layout == DG_LAYOUT_CONTIGUOUS) {
+            mbar_arrive_expect_tx(fb, kStageTx);
             tma_load_3d(a_dst, &tmap_a, fb, 0, p_ti.m0, kb0);
             tma_load_4d(b_dst, &tmap_b, fb, 0, p_ti.n0, kb0, p_ti.g);
         } else {
+            mbar_arrive_expect_tx(fb, kStageTx);
             tma_load_4d(a_dst, &tmap_a, fb, 0, p_ti.m0, kb0, p_ti.g);
             tma_load_4d(b_dst, &tmap_b, fb, 0, p_ti.n0, kb0, p_ti.g);
         }
@@ -376,6 +393,20 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
             p_phase ^= 1u;
         }
     };
+    if (threadIdx.x == 0 && p.layout == DG_LAYOUT_DENSE && p_next()) {
+        // B is the weights: never written by a kernel that lets its
+        // dependents start early (the activation quantiser, the GEMMs), so
+        // its first stages can be copied while the previous kernel of the
+        // stream, typically the quantiser producing A, is still running
+        p_pre = min(STAGES, KP);
+        for (int s = 0; s < p_pre; ++s) {
+            mbar_arrive_expect_tx(full_bar(s), kStageTx);
+            tma_load_3d(sbase + L::kBOff + s * L::kBBytes, &tmap_b, full_bar(s), 0, p_ti.n0, s * KPS);
+            pending |= 1u << s;   // parity 0: the ring's first round
+        }
+    }
+    // the previous kernel in the stream may still be running until here
+    griddep_wait();
     if (threadIdx.x == 0 && p.layout != DG_LAYOUT_MASKED) {
         // the ring is empty: issue the first stage before the CTA barrier, so
         // that its copies overlap the TMEM allocation and the other warps'
