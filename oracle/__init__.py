@@ -7,8 +7,10 @@ under ``moe_grouped_gemm_x128_gb300/``; neither imports the other.
 
 Every function follows the pages "DeepGEMM：一款支持FP8通用矩阵乘法(GEMM)的开源库"
 (功能特色/细粒度缩放功能, 技术细节/两级累加技术, 功能特色/支持多种数据排列方式) and
-the 2kiu.com DeepGEMM tutorial (4.4 精度控制与数值稳定性); the readings taken where
-they are silent are stated in ``oracle.c``.
+the 2kiu.com DeepGEMM tutorial (4.4 精度控制与数值稳定性); the BF16 GEMM and the MX
+functions follow the same tutorial (1, 2.2 and 7) and, for what MX means, the
+OCP Microscaling Formats (MX) v1.0 specification.  The readings taken where the
+pages are silent are stated in ``oracle.c``.
 """
 from __future__ import annotations
 
@@ -68,6 +70,14 @@ def _load():
     lib.oracle_grouped_contiguous.restype = None
     lib.oracle_grouped_masked.argtypes = [P, P, I, P, P, P, P, I, I, I, I]
     lib.oracle_grouped_masked.restype = None
+    lib.oracle_gemm_bf16_nt.argtypes = [P, P, P, I, I, I, P, I]
+    lib.oracle_gemm_bf16_nt.restype = None
+    lib.oracle_ue8m0_decode.argtypes = [ctypes.c_uint8]
+    lib.oracle_ue8m0_decode.restype = ctypes.c_double
+    lib.oracle_quant_mx_1x32.argtypes = [P, I, I, P, P]
+    lib.oracle_quant_mx_1x32.restype = None
+    lib.oracle_gemm_mx_nt.argtypes = [P, P, P, P, P, I, I, I, P, I]
+    lib.oracle_gemm_mx_nt.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = I
     _lib = lib
@@ -260,3 +270,60 @@ def grouped_masked_quant(a, sfa, b, sfb, masked_m, q=None, sfo=None):
 def bf16_bits_to_f32(d: np.ndarray) -> np.ndarray:
     """Widen bf16 bit patterns (uint16) to fp32 exactly."""
     return (d.astype(np.uint32) << 16).view(np.float32)
+
+
+# ------------------------------------------------------------ BF16 GEMM ----
+# A plain GEMM on bf16 operands, the second low-precision format the pages
+# name beside FP8 (2kiu.com tutorial 1 and 2.2): the exact sum of products,
+# rounded once to fp32 and then to bf16 (round to nearest even).
+def gemm_bf16_nt(a_bits, b_bits, rows=None, d=None):
+    """D = A.B^T on bf16 operands.  a_bits uint16 [M,K], b_bits uint16 [N,K]
+    (bf16 bit patterns).  Returns bf16 bits uint16 [M,N]; with ``rows`` only
+    those rows are computed (others keep ``d``'s contents, zero by default)."""
+    M, K = a_bits.shape
+    N = b_bits.shape[0]
+    assert a_bits.dtype == np.uint16 and b_bits.dtype == np.uint16 and b_bits.shape[1] == K
+    if d is None:
+        d = np.zeros((M, N), dtype=np.uint16)
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    _load().oracle_gemm_bf16_nt(_ptr(np.ascontiguousarray(a_bits)), _ptr(np.ascontiguousarray(b_bits)), _ptr(d),
+                                M, N, K, _ptr(r), 0 if r is None else len(r))
+    return d
+
+
+# ------------------------------------------------------ MX (microscaling) --
+# The MX formats the pages point to for finer scale granularity (2kiu.com
+# tutorial 7), as the OCP Microscaling Formats (MX) v1.0 specification
+# defines them: 32 consecutive values along K share one E8M0 scale 2^e.
+MX_BLOCK = 32
+
+
+def ue8m0_decode(code: int) -> float:
+    return _load().oracle_ue8m0_decode(code)
+
+
+def quant_mx_1x32(x: np.ndarray):
+    """MX (E4M3 elements, E8M0 scales) quantiser of the rows of x fp32 [R,K].
+    Returns (q uint8 [R,K], sx uint8 [R,K/32])."""
+    R_, K = x.shape
+    assert K % MX_BLOCK == 0 and x.dtype == np.float32
+    x = np.ascontiguousarray(x)
+    q = np.empty((R_, K), dtype=np.uint8)
+    sx = np.empty((R_, K // MX_BLOCK), dtype=np.uint8)
+    _load().oracle_quant_mx_1x32(_ptr(x), R_, K, _ptr(q), _ptr(sx))
+    return q, sx
+
+
+def gemm_mx_nt(a, sa, b, sb, rows=None, d=None):
+    """MX GEMM D = A.B^T: a uint8 E4M3 [M,K], sa uint8 E8M0 [M,K/32], b [N,K],
+    sb [N,K/32].  Returns bf16 bits uint16 [M,N] (``rows`` as gemm_bf16_nt)."""
+    M, K = a.shape
+    N = b.shape[0]
+    assert K % MX_BLOCK == 0 and sa.shape == (M, K // MX_BLOCK) and sb.shape == (N, K // MX_BLOCK)
+    if d is None:
+        d = np.zeros((M, N), dtype=np.uint16)
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    _load().oracle_gemm_mx_nt(_ptr(np.ascontiguousarray(a)), _ptr(np.ascontiguousarray(sa)),
+                              _ptr(np.ascontiguousarray(b)), _ptr(np.ascontiguousarray(sb)), _ptr(d),
+                              M, N, K, _ptr(r), 0 if r is None else len(r))
+    return d

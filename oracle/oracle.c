@@ -13,6 +13,11 @@
  *        3.3 聚焦FP8, 4.4 精度控制与数值稳定性
  *   [P3] "DeepGEMM：面向大模型的高效矩阵计算加速方案", 四.2 (the per-expert loop
  *        that a grouped GEMM replaces)
+ *   [P4] sections 1 and 2.2 (BF16 as the other low-precision format) and 7
+ *        (MX / micro-scaling formats as the next step); the MX functions
+ *        restate the OCP Microscaling Formats (MX) v1.0 specification (32-value
+ *        blocks sharing an E8M0 power-of-two scale), which the pages point to
+ *        but do not define
  *
  * Readings where the pages are silent (each is listed in the design doc):
  *   - E4M3 for both operands, bias 7, max 448, NaN at 0x7F/0xFF, no infinities.
@@ -21,6 +26,10 @@
  *   - per 128-wide K block, the exact block sum p (in double) is rounded once
  *     to fp32 and promoted with acc = fmaf(p, sfa*sfb, acc), K blocks ascending.
  *   - D = bf16 round-to-nearest-even of acc.
+ *   - BF16 GEMM: the exact sum of products, rounded to fp32, then to bf16.
+ *   - MX: scale exponent floor(log2 amax) - 8 clamped to [-127, 127] (-127 for
+ *     an all-zero block), elements E4M3 RNE saturating at 448; the GEMM is the
+ *     exact sum of scaled 32-block sums, rounded to fp32, then to bf16.
  *
  * Parity pins: every function here is pinned by the CPU tests (closed forms,
  * library conversions, brute force and invariants); none is "parity unpinned".
@@ -345,6 +354,130 @@ void oracle_grouped_masked(const uint8_t *a, const float *sfa, int ldsfa, const 
         gemm_row(a + ((size_t)g * max_m + m) * K, sfa + (size_t)g * KB * ldsfa + m,
                  (size_t)ldsfa, b + (size_t)g * N * K, sfb + (size_t)g * NB * KB, N, K,
                  d + ((size_t)g * max_m + m) * N, NULL);
+    }
+}
+
+/* ------------------------------------------------------------ BF16 GEMM --- */
+
+/* Dense NT GEMM on bf16 operands, no scales (the second low-precision format
+ * the pages name beside FP8: 2kiu.com tutorial 1 and 2.2):
+ *   D[m][n] = bf16_rne(fp32(sum_k a[m][k] * b[n][k])).
+ * The sum is taken in double, which is exact while the products (16
+ * significant bits each) span fewer than 53 - 16 - log2(K) binades, as in
+ * every pinned case; it is rounded once to fp32 (the accumulator type), then
+ * to bf16.
+ *   a bf16 bits [M][K], b bf16 bits [N][K], d bf16 bits [M][N]
+ *   rows optional list of n_rows rows to compute (NULL = all); others untouched. */
+void oracle_gemm_bf16_nt(const uint16_t *a, const uint16_t *b, uint16_t *d, int M, int N, int K,
+                         const int32_t *rows, int n_rows)
+{
+    int count = rows ? n_rows : M;
+    int i;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (i = 0; i < count; ++i) {
+        int m = rows ? rows[i] : i;
+        const uint16_t *a_row = a + (size_t)m * K;
+        int n, k;
+        for (n = 0; n < N; ++n) {
+            const uint16_t *b_row = b + (size_t)n * K;
+            double sum = 0.0;
+            for (k = 0; k < K; ++k)
+                sum += (double)oracle_bf16_to_f32(a_row[k]) * (double)oracle_bf16_to_f32(b_row[k]);
+            d[(size_t)m * N + n] = oracle_bf16_rne((float)sum);
+        }
+    }
+}
+
+/* ------------------------------------------------------ MX (microscaling) --- */
+/* The MX formats the pages point to as the next step after per-group FP8
+ * scaling (2kiu.com tutorial 7: MX / micro-scaling formats with finer scale
+ * granularity), as the OCP Microscaling Formats (MX) specification v1.0
+ * defines them: blocks of 32 consecutive elements share one scale of type
+ * E8M0, a bare power of two. */
+
+#define ORACLE_MX_BLOCK 32
+#define ORACLE_E4M3_EMAX 8 /* exponent of the largest E4M3 power of two (256) */
+
+/* E8M0 scale code c: 2^(c - 127); 0xFF is NaN. */
+double oracle_ue8m0_decode(uint8_t c)
+{
+    if (c == 0xFF)
+        return NAN;
+    return ldexp(1.0, (int)c - 127);
+}
+
+/* MX quantiser of R rows of K values (the specification's conversion of a
+ * vector of scalars to MX, with E4M3 elements):
+ *   per row and 32-wide block along K: amax = max |x|;
+ *   e = floor(log2(amax)) - 8, clamped to [-127, 127] (an all-zero block
+ *   takes e = -127); scale code e + 127;
+ *   q = E4M3 RNE of x / 2^e, saturating at 448 (the block's largest element
+ *   lands in [256, 448]).
+ *   x fp32 [R][K]; q out E4M3 [R][K]; sx out E8M0 [R][K/32] (sx[r*(K/32)+kb]).
+ * x / 2^e is exact whenever it is a normal fp32 number; smaller quotients
+ * encode to +-0 whatever their low bits. */
+void oracle_quant_mx_1x32(const float *x, int R, int K, uint8_t *q, uint8_t *sx)
+{
+    int KB = K / ORACLE_MX_BLOCK;
+    int r;
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < R; ++r) {
+        int kb, k;
+        for (kb = 0; kb < KB; ++kb) {
+            const float *xb = x + (size_t)r * K + (size_t)kb * ORACLE_MX_BLOCK;
+            uint8_t *qb = q + (size_t)r * K + (size_t)kb * ORACLE_MX_BLOCK;
+            double amax = 0.0;
+            int e;
+            for (k = 0; k < ORACLE_MX_BLOCK; ++k)
+                if (fabs((double)xb[k]) > amax)
+                    amax = fabs((double)xb[k]);
+            if (amax == 0.0) {
+                e = -127;
+            } else {
+                int ex;
+                frexp(amax, &ex); /* amax = f * 2^ex, f in [0.5, 1): floor(log2 amax) = ex - 1 */
+                e = ex - 1 - ORACLE_E4M3_EMAX;
+                if (e < -127)
+                    e = -127;
+                if (e > 127)
+                    e = 127;
+            }
+            sx[(size_t)r * KB + kb] = (uint8_t)(e + 127);
+            for (k = 0; k < ORACLE_MX_BLOCK; ++k)
+                qb[k] = oracle_e4m3_encode((float)ldexp((double)xb[k], -e));
+        }
+    }
+}
+
+/* MX GEMM, dense NT:
+ *   D[m][n] = bf16_rne(fp32(sum_kb 2^(sa[m][kb]-127) * 2^(sb[n][kb]-127)
+ *                                 * sum_{k in block kb} dec(a[m][k]) * dec(b[n][k]))),
+ * kb over the 32-wide K blocks.  Every block sum is a multiple of 2^-18 below
+ * 2^23 and the scales are powers of two, so the double sum is exact while the
+ * scaled block sums span fewer than ~30 binades (every pinned case); it is
+ * rounded once to fp32, then to bf16.
+ *   a E4M3 [M][K], sa E8M0 [M][K/32], b E4M3 [N][K], sb E8M0 [N][K/32],
+ *   d bf16 bits [M][N]; rows as in oracle_gemm_bf16_nt. */
+void oracle_gemm_mx_nt(const uint8_t *a, const uint8_t *sa, const uint8_t *b, const uint8_t *sb,
+                       uint16_t *d, int M, int N, int K, const int32_t *rows, int n_rows)
+{
+    int KB = K / ORACLE_MX_BLOCK;
+    int count = rows ? n_rows : M;
+    int i;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (i = 0; i < count; ++i) {
+        int m = rows ? rows[i] : i;
+        int n, kb, k;
+        for (n = 0; n < N; ++n) {
+            double sum = 0.0;
+            for (kb = 0; kb < KB; ++kb) {
+                double p = 0.0;
+                for (k = kb * ORACLE_MX_BLOCK; k < (kb + 1) * ORACLE_MX_BLOCK; ++k)
+                    p += g_dec[a[(size_t)m * K + k]] * g_dec[b[(size_t)n * K + k]];
+                sum += p * oracle_ue8m0_decode(sa[(size_t)m * KB + kb]) * oracle_ue8m0_decode(sb[(size_t)n * KB + kb]);
+            }
+            d[(size_t)m * N + n] = oracle_bf16_rne((float)sum);
+        }
     }
 }
 
