@@ -142,6 +142,58 @@ def _ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
 
 
+# Argument checks.  The C entry points take bare pointers, so a tensor of the
+# wrong size, type, layout or device would make the kernels read or write
+# outside it; every binding below checks each tensor against the sizes taken
+# from its first operand before calling the library.
+_dt = {}
+
+
+def _dtypes():
+    if not _dt:
+        import torch
+        _dt.update(fp8=(torch.uint8, torch.float8_e4m3fn), f32=(torch.float32,), bf16=(torch.bfloat16,),
+                   i32=(torch.int32,), act=(torch.float32, torch.bfloat16))
+    return _dt
+
+
+def _dims(t, name: str, ndim: int):
+    try:
+        shape = t.shape
+    except AttributeError:
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}") from None
+    if len(shape) != ndim:
+        raise ValueError(f"{name}: expected {ndim} dimensions, got shape {tuple(shape)}")
+    return shape
+
+
+def _want(t, name: str, shape: tuple, dtypes: tuple) -> None:
+    try:
+        ok = t.shape == shape and t.dtype in dtypes and t.is_contiguous()
+    except AttributeError:
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}") from None
+    if not ok:
+        if tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+        if t.dtype not in dtypes:
+            raise TypeError(f"{name}: expected dtype {' or '.join(str(d) for d in dtypes)}, got {t.dtype}")
+        raise ValueError(f"{name}: must be contiguous")
+
+
+def _on_device(*named) -> None:
+    """Every tensor on the current CUDA device (where the library launches)."""
+    dev = None
+    for name, t in named:
+        idx = t.get_device()
+        if idx < 0:
+            raise ValueError(f"{name}: a CUDA tensor is required (there is no CPU path), got one on {t.device}")
+        if dev is None:
+            import torch
+            dev = torch._C._cuda_getDevice()
+        if idx != dev:
+            raise ValueError(f"{name}: on cuda:{idx}, but the current device is cuda:{dev}")
+
+
 def round_up(x: int, m: int) -> int:
     return (x + m - 1) // m * m
 
@@ -151,15 +203,25 @@ def dg_quant_act_1x128(x, q=None, sfa=None, stream=None):
     """Per-token 1x128 quantiser.  x: CUDA fp32 or bf16 [M, K].
     Returns (q uint8 [M, K], sfa fp32 [K/128, round_up(M, 4)])."""
     import torch
-    M, K = x.shape
+    T = _dtypes()
+    M, K = _dims(x, "x", 2)
     if q is None:
         q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
     if sfa is None:
         sfa = torch.zeros((K // QBLOCK, round_up(M, 4)), dtype=torch.float32, device=x.device)
-    dt = {torch.float32: DG_DTYPE_F32, torch.bfloat16: DG_DTYPE_BF16}.get(x.dtype)
-    if dt is None:
-        raise TypeError(f"unsupported activation dtype {x.dtype}")
-    assert x.is_contiguous() and q.is_contiguous() and sfa.is_contiguous()
+    # one expression on the common path; the per-tensor checks name the culprit
+    try:
+        ok = (x.dtype in T["act"] and q.dtype in T["fp8"] and sfa.dtype in T["f32"] and q.shape == (M, K)
+              and sfa.shape == (K // QBLOCK, round_up(M, 4)) and x.is_contiguous() and q.is_contiguous()
+              and sfa.is_contiguous())
+    except AttributeError:
+        ok = False
+    if not ok:
+        _want(x, "x", (M, K), T["act"])
+        _want(q, "q", (M, K), T["fp8"])
+        _want(sfa, "sfa", (K // QBLOCK, round_up(M, 4)), T["f32"])
+    _on_device(("x", x), ("q", q), ("sfa", sfa))
+    dt = DG_DTYPE_F32 if x.dtype == torch.float32 else DG_DTYPE_BF16
     _check("dg_quant_act_1x128", load().dg_quant_act_1x128(_ptr(x), dt, _ptr(q), _ptr(sfa), M, K, _stream(stream)))
     return q, sfa
 
@@ -168,27 +230,60 @@ def dg_quant_weight_128x128(w, q=None, sfb=None, stream=None):
     """Per-block 128x128 quantiser.  w: CUDA fp32 [N, K] or [G, N, K].
     Returns (q uint8 like w, sfb fp32 [(G,) ceil(N/128), K/128])."""
     import torch
+    T = _dtypes()
+    if not isinstance(w, torch.Tensor) or w.dim() not in (2, 3):
+        raise ValueError("w: expected a [N, K] or [G, N, K] torch.Tensor")
     squeeze = w.dim() == 2
     w3 = w.unsqueeze(0) if squeeze else w
     G, N, K = w3.shape
+    _want(w3, "w", (G, N, K), T["f32"])
     if q is None:
         q = torch.empty(w3.shape, dtype=torch.uint8, device=w.device)
+    elif squeeze:
+        q = q.unsqueeze(0)
     if sfb is None:
         sfb = torch.empty((G, (N + QBLOCK - 1) // QBLOCK, K // QBLOCK), dtype=torch.float32, device=w.device)
-    assert w3.is_contiguous() and w3.dtype == torch.float32
+    elif squeeze:
+        sfb = sfb.unsqueeze(0)
+    _want(q, "q", (G, N, K), T["fp8"])
+    _want(sfb, "sfb", (G, (N + QBLOCK - 1) // QBLOCK, K // QBLOCK), T["f32"])
+    _on_device(("w", w3), ("q", q), ("sfb", sfb))
     _check("dg_quant_weight_128x128",
            load().dg_quant_weight_128x128(_ptr(w3), _ptr(q), _ptr(sfb), G, N, K, _stream(stream)))
     return (q[0], sfb[0]) if squeeze else (q, sfb)
 
 
 # ------------------------------------------------------------------ GEMMs --
+def _grouped_operands(T, a, sfa, b, sfb, sfa_shape, G, N, K):
+    _want(a, "a", tuple(a.shape), T["fp8"])
+    _want(sfa, "sfa", sfa_shape, T["f32"])
+    _want(b, "b", (G, N, K), T["fp8"])
+    _want(sfb, "sfb", (G, -(-N // QBLOCK), K // QBLOCK), T["f32"])
+
+
 def dg_fp8_gemm_nt(a, sfa, b, sfb, d=None, stream=None):
     """Dense D = A . B^T (bf16 [M, N])."""
     import torch
-    M, K = a.shape
-    N = b.shape[0]
+    T = _dtypes()
+    M, K = _dims(a, "a", 2)
+    N = _dims(b, "b", 2)[0]
     if d is None:
         d = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    fp8, f32 = T["fp8"], T["f32"]
+    try:
+        ok = (a.dtype in fp8 and b.dtype in fp8 and sfa.dtype in f32 and sfb.dtype in f32
+              and d.dtype in T["bf16"] and b.shape == (N, K) and sfa.shape == (K // QBLOCK, round_up(M, 4))
+              and sfb.shape == (-(-N // QBLOCK), K // QBLOCK) and d.shape == (M, N) and a.is_contiguous()
+              and b.is_contiguous() and sfa.is_contiguous() and sfb.is_contiguous() and d.is_contiguous())
+    except AttributeError:
+        ok = False
+    if not ok:
+        _want(a, "a", (M, K), fp8)
+        _want(sfa, "sfa", (K // QBLOCK, round_up(M, 4)), f32)
+        _want(b, "b", (N, K), fp8)
+        _want(sfb, "sfb", (-(-N // QBLOCK), K // QBLOCK), f32)
+        _want(d, "d", (M, N), T["bf16"])
+    _on_device(("a", a), ("sfa", sfa), ("b", b), ("sfb", sfb), ("d", d))
     _check("dg_fp8_gemm_nt", load().dg_fp8_gemm_nt(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(d), M, N, K,
                                                    _stream(stream)))
     return d
@@ -197,10 +292,15 @@ def dg_fp8_gemm_nt(a, sfa, b, sfb, d=None, stream=None):
 def dg_fp8_grouped_contiguous(a, sfa, b, sfb, m_indices, d=None, stream=None):
     """Contiguous MoE layout: a [sum_M, K], b [G, N, K], m_indices int32 [sum_M]."""
     import torch
-    sum_M, K = a.shape
-    G, N, _ = b.shape
+    T = _dtypes()
+    sum_M, K = _dims(a, "a", 2)
+    G, N, _ = _dims(b, "b", 3)
+    _grouped_operands(T, a, sfa, b, sfb, (K // QBLOCK, round_up(sum_M, 4)), G, N, K)
+    _want(m_indices, "m_indices", (sum_M,), T["i32"])
     if d is None:
         d = torch.empty((sum_M, N), dtype=torch.bfloat16, device=a.device)
+    _want(d, "d", (sum_M, N), T["bf16"])
+    _on_device(("a", a), ("sfa", sfa), ("b", b), ("sfb", sfb), ("m_indices", m_indices), ("d", d))
     _check("dg_fp8_grouped_contiguous",
            load().dg_fp8_grouped_contiguous(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(d), _ptr(m_indices),
                                             sum_M, N, K, G, _stream(stream)))
@@ -211,10 +311,15 @@ def dg_fp8_grouped_masked(a, sfa, b, sfb, masked_m, d=None, expected_m: int = 0,
     """Masked MoE layout: a [G, max_m, K], b [G, N, K], masked_m int32 [G] on
     the device; rows >= masked_m[g] of d are left untouched."""
     import torch
-    G, max_m, K = a.shape
-    N = b.shape[1]
+    T = _dtypes()
+    G, max_m, K = _dims(a, "a", 3)
+    N = _dims(b, "b", 3)[1]
+    _grouped_operands(T, a, sfa, b, sfb, (G, K // QBLOCK, round_up(max_m, 4)), G, N, K)
+    _want(masked_m, "masked_m", (G,), T["i32"])
     if d is None:
         d = torch.empty((G, max_m, N), dtype=torch.bfloat16, device=a.device)
+    _want(d, "d", (G, max_m, N), T["bf16"])
+    _on_device(("a", a), ("sfa", sfa), ("b", b), ("sfb", sfb), ("masked_m", masked_m), ("d", d))
     _check("dg_fp8_grouped_masked",
            load().dg_fp8_grouped_masked(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(d), _ptr(masked_m), G, max_m,
                                         N, K, expected_m, _stream(stream)))
@@ -224,20 +329,28 @@ def dg_fp8_grouped_masked(a, sfa, b, sfb, masked_m, d=None, expected_m: int = 0,
 # --------------------------------------------- GEMMs, re-quantised output --
 def _qout(shape, rows_ld: int, groups_shape, device, q, sfo):
     import torch
+    T = _dtypes()
     if q is None:
         q = torch.empty(shape, dtype=torch.uint8, device=device)
     if sfo is None:
         sfo = torch.zeros((*groups_shape, rows_ld), dtype=torch.float32, device=device)
-    assert q.is_contiguous() and sfo.is_contiguous()
+    _want(q, "q", tuple(shape), T["fp8"])
+    _want(sfo, "sfo", (*groups_shape, rows_ld), T["f32"])
     return q, sfo
 
 
 def dg_fp8_gemm_nt_q(a, sfa, b, sfb, q=None, sfo=None, stream=None):
     """Dense D = A . B^T re-quantised: returns (q uint8 [M, N],
     sfo fp32 [N/128, round_up(M, 4)])."""
-    M, K = a.shape
-    N = b.shape[0]
+    T = _dtypes()
+    M, K = _dims(a, "a", 2)
+    N = _dims(b, "b", 2)[0]
+    _want(a, "a", (M, K), T["fp8"])
+    _want(sfa, "sfa", (K // QBLOCK, round_up(M, 4)), T["f32"])
+    _want(b, "b", (N, K), T["fp8"])
+    _want(sfb, "sfb", (-(-N // QBLOCK), K // QBLOCK), T["f32"])
     q, sfo = _qout((M, N), round_up(M, 4), (N // QBLOCK,), a.device, q, sfo)
+    _on_device(("a", a), ("sfa", sfa), ("b", b), ("sfb", sfb), ("q", q), ("sfo", sfo))
     _check("dg_fp8_gemm_nt_q", load().dg_fp8_gemm_nt_q(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(q), _ptr(sfo),
                                                        M, N, K, _stream(stream)))
     return q, sfo
@@ -246,9 +359,13 @@ def dg_fp8_gemm_nt_q(a, sfa, b, sfb, q=None, sfo=None, stream=None):
 def dg_fp8_grouped_contiguous_q(a, sfa, b, sfb, m_indices, q=None, sfo=None, stream=None):
     """Contiguous MoE layout, re-quantised: returns (q uint8 [sum_M, N],
     sfo fp32 [N/128, sum_M]); rows with index -1 are left untouched."""
-    sum_M, K = a.shape
-    G, N, _ = b.shape
+    T = _dtypes()
+    sum_M, K = _dims(a, "a", 2)
+    G, N, _ = _dims(b, "b", 3)
+    _grouped_operands(T, a, sfa, b, sfb, (K // QBLOCK, round_up(sum_M, 4)), G, N, K)
+    _want(m_indices, "m_indices", (sum_M,), T["i32"])
     q, sfo = _qout((sum_M, N), sum_M, (N // QBLOCK,), a.device, q, sfo)
+    _on_device(("a", a), ("sfa", sfa), ("b", b), ("sfb", sfb), ("m_indices", m_indices), ("q", q), ("sfo", sfo))
     _check("dg_fp8_grouped_contiguous_q",
            load().dg_fp8_grouped_contiguous_q(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(q), _ptr(sfo),
                                               _ptr(m_indices), sum_M, N, K, G, _stream(stream)))
@@ -259,9 +376,13 @@ def dg_fp8_grouped_masked_q(a, sfa, b, sfb, masked_m, q=None, sfo=None, expected
     """Masked MoE layout, re-quantised: returns (q uint8 [G, max_m, N],
     sfo fp32 [G, N/128, round_up(max_m, 4)]); rows >= masked_m[g] are left
     untouched."""
-    G, max_m, K = a.shape
-    N = b.shape[1]
+    T = _dtypes()
+    G, max_m, K = _dims(a, "a", 3)
+    N = _dims(b, "b", 3)[1]
+    _grouped_operands(T, a, sfa, b, sfb, (G, K // QBLOCK, round_up(max_m, 4)), G, N, K)
+    _want(masked_m, "masked_m", (G,), T["i32"])
     q, sfo = _qout((G, max_m, N), round_up(max_m, 4), (G, N // QBLOCK), a.device, q, sfo)
+    _on_device(("a", a), ("sfa", sfa), ("b", b), ("sfb", sfb), ("masked_m", masked_m), ("q", q), ("sfo", sfo))
     _check("dg_fp8_grouped_masked_q",
            load().dg_fp8_grouped_masked_q(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(q), _ptr(sfo),
                                           _ptr(masked_m), G, max_m, N, K, expected_m, _stream(stream)))
