@@ -19,7 +19,7 @@
  *        blocks sharing an E8M0 power-of-two scale), which the pages point to
  *        but do not define
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   - E4M3 for both operands, bias 7, max 448, NaN at 0x7F/0xFF, no infinities.
  *   - scale s = max(amax, 1e-4) / 448 in fp32 (IEEE division); q = RNE-saturating
  *     E4M3 encode of fp32(x / s).
