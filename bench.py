@@ -2,9 +2,11 @@
 
 One step = the whole path over one batch: 1x128 quantisation of the fp32
 activations (dg_quant_act_1x128) followed by the FP8 GEMM with two-level
-accumulation and bf16 output (dg_fp8_gemm_nt); the weights are quantised once,
-offline, before timing (dg_quant_weight_128x128).  Default workload: the
-skinny dense GEMM M=256, N=7168, K=2048 with 1% x20 outliers in A.
+accumulation and bf16 output; the weights are quantised once, offline, before
+timing (dg_quant_weight_128x128).  The headline workload is the largest one
+that fits one GPU: the contiguous MoE grouped GEMM (G=8 experts, 32768 routed
+tokens, N=4096, K=7168).  Every other workload's GEMM (and quantiser, where
+it has one) is timed in the same run and reported under "configs".
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on the
 host cores instead (a bounded row sample of the same workload).
@@ -34,20 +36,26 @@ FP8_PER_BF16 = 2.0           # nominal dense fp8 : bf16 tensor ratio (4.5 : 2.25
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 2 ** 20
+HEADLINE = "contig"
+EXTRA = ("tiny", "skinny", "sweep_n7168_k18432", "sweep_n24576_k1536", "sweep_n2112_k7168", "masked")
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="dg", choices=["dg", "reference"])
-    ap.add_argument("--workload", default="skinny", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="contiguous workload: routed tokens (0 = the workload's 32768); a profiling aid")
     ap.add_argument("--shape", default="", help="M,N,K: a dense problem of this shape instead of the workload "
                                                  "(profiling aid; not a bench line)")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def peaks():
@@ -118,13 +126,21 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- workload ---
+def with_tokens(w: wl.Workload, tokens: int) -> wl.Workload:
+    if not tokens or w.layout != "contiguous":
+        return w
+    return wl.Workload(f"{w.name}_t{tokens}", w.layout, N=w.N, K=w.K, G=w.G, tokens=tokens, seed=w.seed)
+
+
 def describe(w: wl.Workload) -> str:
     if w.layout == "dense":
         return (f"dense NT FP8 GEMM M={w.M} N={w.N} K={w.K}" + (" (1% x20 outliers in A)" if w.outliers else "")
                 + "; step = 1x128 activation quantisation + GEMM")
     if w.layout == "contiguous":
-        return f"MoE contiguous FP8 GEMM G={w.G} tokens={w.tokens} N={w.N} K={w.K}; step = quantisation + GEMM"
-    return f"MoE masked FP8 GEMM G={w.G} max_m={w.max_m} N={w.N} K={w.K}; step = quantisation + GEMM"
+        return (f"MoE contiguous grouped FP8 GEMM G={w.G} tokens={w.tokens} N={w.N} K={w.K} (expert popularity "
+                f"spanning 10x, segments padded to 128 rows); step = 1x128 activation quantisation + GEMM")
+    return (f"MoE masked grouped FP8 GEMM G={w.G} max_m={w.max_m} N={w.N} K={w.K}, masked_m ~ U{{0..{w.max_m}}} "
+            f"on the device; CUDA-graph captured GEMM")
 
 
 def gemm_shape(w: wl.Workload):
@@ -136,6 +152,12 @@ def gemm_shape(w: wl.Workload):
         return len(m_indices), int(counts.sum()), w.N, w.K, w.G
     mm = wl.masked_counts(w.G, w.max_m, w.seed)
     return w.G * w.max_m, int(mm.sum()), w.N, w.K, w.G
+
+
+def useful_flops(w: wl.Workload) -> float:
+    """2 M N K over the useful rows only (padding rows and masked tails excluded)."""
+    _, useful, N, K, _ = gemm_shape(w)
+    return 2.0 * useful * N * K
 
 
 def algorithmic_bytes(w: wl.Workload):
@@ -150,6 +172,25 @@ def algorithmic_bytes(w: wl.Workload):
     else:
         experts = G
     return useful * K + experts * N * K + useful * KB * 4 + experts * NB * KB * 4 + useful * N * 2
+
+
+def quant_bytes(rows: int, K: int, in_bytes: int = 4) -> int:
+    """Bytes the activation quantiser must move: the input once, the codes and
+    one fp32 scale per 128 values."""
+    return rows * K * in_bytes + rows * K + rows * (K // 128) * 4
+
+
+def roofline(flops: float, nbytes: float, seconds: float, hbm: float, fp8_peak: float) -> dict:
+    """The slower of compute at the FP8 peak and the bytes over HBM decides
+    the bound; achieved is the work of that bound over the measured time."""
+    t_mem = nbytes / (hbm * 1e9)
+    t_cmp = flops / (fp8_peak * 1e12)
+    if t_mem >= t_cmp:
+        r = {"bound": "hbm", "achieved": nbytes / seconds / 1e9, "peak": hbm, "unit": "GB/s"}
+    else:
+        r = {"bound": "tensor", "achieved": flops / seconds / 1e12, "peak": fp8_peak, "unit": "TFLOP/s"}
+    r["frac"] = r["achieved"] / r["peak"]
+    return r
 
 
 # -------------------------------------------------------- ncu traffic ------
@@ -209,24 +250,60 @@ def job_throughput(world: int, units_per_rank_step: float, steps: int, max_ms: f
 
 
 # ---------------------------------------------------------------- CPU leg --
-def cpu_oracle_rate(w: wl.Workload, seconds: float):
-    """Time the oracle (quantise + GEMM) over whole rows of the workload,
-    repeating the full row range until about `seconds` have passed; returns
-    (TFLOP/s, rows computed, elapsed s, threads)."""
+def _contig_sample_setup(w: wl.Workload):
     import oracle
-    if w.layout != "dense":
-        raise SystemExit("the CPU baseline leg covers the dense workloads")
-    x, wt = wl.dense_inputs(w.M, w.N, w.K, w.seed, w.outliers)
+    x, wt, m_indices, counts = wl.contiguous_inputs(w)
     qb, sfb = oracle.quant_weight_128x128(wt)
+    a_full = np.zeros((len(m_indices), w.K), np.uint8)
+    sfa_full = np.zeros((w.K // 128, oracle.round_up(len(m_indices), 4)), np.float32)
+    valid = np.flatnonzero(m_indices >= 0)
+    return x, qb, sfb, m_indices, a_full, sfa_full, valid
+
+
+def _oracle_rows(w: wl.Workload, state, rows: np.ndarray):
+    """The oracle's quantise + GEMM over the listed rows of the workload
+    (contiguous: the listed rows' activations quantised into the full-size
+    operand, then the grouped GEMM restricted to those rows)."""
+    import oracle
+    if w.layout == "dense":
+        x, qb, sfb = state
+        qa, sfa = oracle.quant_act_1x128(x[rows])
+        oracle.gemm_nt(qa, sfa, qb, sfb)
+        return
+    x, qb, sfb, m_indices, a_full, sfa_full, _ = state
+    qa, sfa = oracle.quant_act_1x128(x[rows])
+    a_full[rows] = qa
+    sfa_full[:, rows] = sfa[:, :len(rows)]
+    oracle.grouped_contiguous(a_full, sfa_full, qb, sfb, m_indices, rows=rows)
+
+
+def _oracle_state(w: wl.Workload):
+    import oracle
+    if w.layout == "dense":
+        x, wt = wl.dense_inputs(w.M, w.N, w.K, w.seed, w.outliers)
+        qb, sfb = oracle.quant_weight_128x128(wt)
+        return (x, qb, sfb), np.arange(w.M)
+    if w.layout == "contiguous":
+        st = _contig_sample_setup(w)
+        return st, st[-1]
+    raise SystemExit("the CPU leg covers the dense and contiguous workloads")
+
+
+def cpu_oracle_rate(w: wl.Workload, seconds: float):
+    """Time the oracle (quantise + GEMM) over useful rows of the workload, in
+    growing chunks walking through a seeded permutation of them, until about
+    `seconds` have passed; returns (TFLOP/s, rows computed, elapsed s, threads)."""
+    import oracle
+    state, rows_all = _oracle_state(w)
+    order = np.random.default_rng(99).permutation(rows_all)
     rows_done, elapsed, chunk, r0 = 0, 0.0, 8, 0
     while elapsed < seconds:
-        r1 = min(w.M, r0 + chunk)
+        rows = np.sort(order[r0:r0 + chunk]).astype(np.int32)
         t0 = time.perf_counter()
-        qa, sfa = oracle.quant_act_1x128(x[r0:r1])
-        oracle.gemm_nt(qa, sfa, qb, sfb)
+        _oracle_rows(w, state, rows)
         elapsed += time.perf_counter() - t0
-        rows_done += r1 - r0
-        r0 = 0 if r1 >= w.M else r1
+        rows_done += len(rows)
+        r0 = 0 if r0 + chunk >= len(order) else r0 + chunk
         chunk = min(chunk * 2, 64)
     flops = 2.0 * rows_done * w.N * w.K
     return flops / elapsed / 1e12, rows_done, elapsed, oracle.num_threads()
@@ -234,39 +311,29 @@ def cpu_oracle_rate(w: wl.Workload, seconds: float):
 
 def run_reference(args, w):
     """The oracle as it stands, timed on the host cores: every step quantises
-    and multiplies a bounded sample of the workload (up to one row per oracle
-    thread, and as many output columns as fit the per-step share of a two
-    minute budget); the value is the sampled FLOPs over the sampled time."""
+    and multiplies a bounded sample of the workload's useful rows (one row
+    per oracle thread, walking through a seeded permutation), so that the
+    whole run stays within a few minutes; the value is the sampled FLOPs over
+    the sampled time."""
     import oracle
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    if w.layout != "dense":
-        raise SystemExit("the CPU reference arm covers the dense workloads")
-    x, wt = wl.dense_inputs(w.M, w.N, w.K, w.seed, w.outliers)
-    qb, sfb = oracle.quant_weight_128x128(wt)
+    state, rows_all = _oracle_state(w)
     thr = oracle.num_threads()
-    rows = min(w.M, thr)
-    per_step = 120.0 / (args.steps + args.warmup)
-    # calibrate the output-element rate on one 128-column slice
-    t0 = time.perf_counter()
-    qa, sfa = oracle.quant_act_1x128(x[:rows])
-    oracle.gemm_nt(qa, sfa, qb[:128], sfb[:1])
-    rate = rows * 128 / max(time.perf_counter() - t0, 1e-6)
-    cols = int(max(8, min(w.N, rate * per_step / rows)) // 8 * 8)
-    nbs = -(-cols // 128)
+    rows_per_step = min(len(rows_all), thr)
+    order = np.random.default_rng(99).permutation(rows_all)
     flops = 0.0
     elapsed = 0.0
     for i in range(args.warmup + args.steps):
-        r0 = (i * rows) % w.M
-        xr = x[r0:r0 + rows]
+        r0 = (i * rows_per_step) % max(len(order) - rows_per_step + 1, 1)
+        rows = np.sort(order[r0:r0 + rows_per_step]).astype(np.int32)
         t0 = time.perf_counter()
-        qa, sfa = oracle.quant_act_1x128(xr)
-        oracle.gemm_nt(qa, sfa, np.ascontiguousarray(qb[:cols]), np.ascontiguousarray(sfb[:nbs]))
+        _oracle_rows(w, state, rows)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             elapsed += dt
-            flops += 2.0 * len(xr) * cols * w.K
+            flops += 2.0 * len(rows) * w.N * w.K
     value = flops / elapsed / 1e12
     rows_total = gemm_shape(w)[0]
     line = {
@@ -275,7 +342,7 @@ def run_reference(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 block sums, fp32 promotion",
         "data": "synthetic", "config": {"workload": describe(w)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
-                         "sample": f"per step {rows} of {rows_total} rows x {cols} of {w.N} columns "
+                         "sample": f"per step {rows_per_step} of {rows_total} rows x all {w.N} columns "
                                    f"(quantise + GEMM), {elapsed:.1f} s timed"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -283,6 +350,138 @@ def run_reference(args, w):
 
 
 # ---------------------------------------------------------------- GPU leg --
+class Case:
+    """One workload resident on the device, in `n_sets` independent copies of
+    the per-step tensors (activations, codes, scales, output) so that steps
+    rotating through them exceed L2; weights are shared."""
+
+    def __init__(self, dg, torch, w: wl.Workload, dev, min_sets: int = 1):
+        self.w = w
+        self.dg = dg
+        self.torch = torch
+        rows, useful, N, K, G = gemm_shape(w)
+        self.rows, self.useful, self.N, self.K, self.G = rows, useful, N, K, G
+        self.flops = useful_flops(w)
+        self.bytes = algorithmic_bytes(w)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        if w.layout == "dense":
+            x, wt = wl.dense_inputs(w.M, N, K, w.seed, w.outliers)
+            self.meta = None
+        elif w.layout == "contiguous":
+            x, wt, m_indices, _ = wl.contiguous_inputs(w)
+            self.meta = t(m_indices)
+        else:
+            x, wt, masked_m = wl.masked_inputs(w)
+            self.meta = t(masked_m)
+        self.x_host = x
+        wdev = t(wt)
+        self.qb, self.sfb = dg.dg_quant_weight_128x128(wdev)
+        del wdev
+        set_bytes = x.nbytes + rows * K + rows * N * 2
+        self.set_bytes = set_bytes
+        self.n_sets = max(min_sets, -(-2 * L2_BYTES // set_bytes))
+        self.xs, self.qas, self.sfas, self.ds = [], [], [], []
+        xdev = t(x)
+        for i in range(self.n_sets):
+            self.xs.append(xdev if i == 0 else xdev.clone())
+            if w.layout == "masked":
+                qa = torch.empty((G, w.max_m, K), dtype=torch.uint8, device=dev)
+                sfa = torch.zeros((G, K // 128, dg.round_up(w.max_m, 4)), dtype=torch.float32, device=dev)
+                for e in range(G):   # per-expert quantisation (set-up, untimed)
+                    dg.dg_quant_act_1x128(self.xs[i][e], qa[e], sfa[e])
+                d = torch.empty((G, w.max_m, N), dtype=torch.bfloat16, device=dev)
+            else:
+                qa = torch.empty((rows, K), dtype=torch.uint8, device=dev)
+                sfa = torch.zeros((K // 128, dg.round_up(rows, 4)), dtype=torch.float32, device=dev)
+                d = torch.empty((rows, N), dtype=torch.bfloat16, device=dev)
+            self.qas.append(qa)
+            self.sfas.append(sfa)
+            self.ds.append(d)
+        torch.cuda.synchronize()
+
+    @property
+    def has_quant(self) -> bool:
+        return self.w.layout != "masked"
+
+    def quant(self, j: int, stream=None):
+        j %= self.n_sets
+        self.dg.dg_quant_act_1x128(self.xs[j], self.qas[j], self.sfas[j], stream=stream)
+
+    def gemm(self, j: int, stream=None):
+        j %= self.n_sets
+        dg = self.dg
+        if self.w.layout == "dense":
+            dg.dg_fp8_gemm_nt(self.qas[j], self.sfas[j], self.qb, self.sfb, self.ds[j], stream=stream)
+        elif self.w.layout == "contiguous":
+            dg.dg_fp8_grouped_contiguous(self.qas[j], self.sfas[j], self.qb, self.sfb, self.meta, self.ds[j],
+                                         stream=stream)
+        else:
+            dg.dg_fp8_grouped_masked(self.qas[j], self.sfas[j], self.qb, self.sfb, self.meta, self.ds[j],
+                                     expected_m=self.w.max_m // 2, stream=stream)
+
+    def step(self, j: int, stream=None):
+        if self.has_quant:
+            self.quant(j, stream)
+        self.gemm(j, stream)
+
+    def l2_note(self) -> str:
+        if self.n_sets > 1:
+            return f"rotating {self.n_sets} input sets of {self.set_bytes / 1e6:.1f} MB (> 2x L2) between launches"
+        return f"inputs of {self.set_bytes / 1e6:.0f} MB per step (> 2x L2)"
+
+
+def graph_time_ms(torch, body, launches: int, reps: int) -> float:
+    """Average device time of one `body(i)` call: a CUDA graph of `launches`
+    calls (rotating i) is captured, replayed once untimed, then `reps` times
+    between CUDA events on the replaying stream."""
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        for i in range(launches):
+            body(i)
+    g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / (launches * reps)
+
+
+def extra_config(torch, dg, name: str, dev, hbm: float, fp8_peak: float) -> dict:
+    """GEMM (and quantiser) device time of one more workload, from CUDA-graph
+    replays rotating over input sets larger than 2x L2."""
+    w = wl.WORKLOADS[name]
+    c = Case(dg, torch, w, dev)
+    launches = max(c.n_sets, 8) if c.n_sets > 1 else 8
+    for i in range(3):
+        c.step(i)
+    torch.cuda.synchronize()
+    gemm_ms = graph_time_ms(torch, c.gemm, launches, max(1, 200 // launches))
+    r = roofline(c.flops, c.bytes, gemm_ms * 1e-3, hbm, fp8_peak)
+    out = {"workload": describe(w), "kernel": "fp8_gemm_kernel", "kernel_us": gemm_ms * 1e3,
+           "tflops": c.flops / (gemm_ms * 1e-3) / 1e12, "useful_flop": c.flops, "algorithmic_bytes": c.bytes, **r,
+           "plan": dg.dg_query_plan({"dense": 0, "contiguous": 1, "masked": 2}[w.layout],
+                                    w.max_m if w.layout == "masked" else c.rows, c.N, c.K, c.G),
+           "l2": c.l2_note(), "timing": f"CUDA graph of {launches} launches, replayed"}
+    if w.layout == "masked":
+        out["masked_m_sum"] = c.useful
+    if c.has_quant:
+        q_ms = graph_time_ms(torch, c.quant, launches, max(1, 200 // launches))
+        qb = quant_bytes(c.rows, c.K)
+        out["quant_us"] = q_ms * 1e3
+        out["quant_gbs"] = qb / (q_ms * 1e-3) / 1e9
+        out["quant_frac_hbm"] = out["quant_gbs"] / hbm
+    del c
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args, w):
     import torch
     import torch.distributed as dist
@@ -297,182 +496,167 @@ def run_gpu(args, w):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dg.build()
     dg.load()
-    if w.layout != "dense":
-        raise SystemExit("bench.py times the dense workloads; grouped layouts are covered by the tests")
-    M, N, K = w.M, w.N, w.K
     dev = torch.device("cuda", local)
+    hbm, bf16, bf16_sus, src = peaks()
+    fp8_peak = bf16 * FP8_PER_BF16
 
-    # inputs: several independent sets so that consecutive steps do not hit L2
-    x_host, w_host = wl.dense_inputs(M, N, K, w.seed, w.outliers)
-    set_bytes = M * K * 4 + M * K + N * K + M * N * 2
-    n_sets = max(2, -(-2 * L2_BYTES // set_bytes))
-    xs, qas, sfas, qbs, sfbs, ds = [], [], [], [], [], []
-    wt = torch.from_numpy(w_host).to(dev)
-    for i in range(n_sets):
-        xs.append(torch.from_numpy(x_host).to(dev))
-        qb, sfb = dg.dg_quant_weight_128x128(wt)
-        qbs.append(qb)
-        sfbs.append(sfb)
-        qas.append(torch.empty((M, K), dtype=torch.uint8, device=dev))
-        sfas.append(torch.zeros((K // 128, dg.round_up(M, 4)), dtype=torch.float32, device=dev))
-        ds.append(torch.empty((M, N), dtype=torch.bfloat16, device=dev))
-    del wt
-    torch.cuda.synchronize()
+    c = Case(dg, torch, w, dev)
     stream = torch.cuda.current_stream()
-
-    def quant(i):
-        j = i % n_sets
-        dg.dg_quant_act_1x128(xs[j], qas[j], sfas[j])
-
-    def gemm(i):
-        j = i % n_sets
-        dg.dg_fp8_gemm_nt(qas[j], sfas[j], qbs[j], sfbs[j], ds[j])
-
-    def step(i):
-        quant(i)
-        gemm(i)
-
     for i in range(args.warmup):
-        step(i)
+        c.step(i)
     torch.cuda.synchronize()
 
-    # The steps are launched from a CUDA graph (host launch cost would
-    # otherwise dominate microsecond kernels): one graph holds `chunk` steps
-    # over the rotating input sets and is replayed until `steps` steps have run.
-    chunk = min(args.steps, 100)
-    reps = -(-args.steps // chunk)
-    steps_run = chunk * reps
-
-    def capture(body):
-        cap = torch.cuda.Stream()
-        cap.wait_stream(torch.cuda.current_stream())
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=cap):
-            for i in range(chunk):
-                body(i)
-        g.replay()
-        torch.cuda.synchronize()
-        return g
-
-    def timed(graph, n):
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        t0.record(stream)
-        for _ in range(n):
-            graph.replay()
-        t1.record(stream)
-        torch.cuda.synchronize()
-        return t0.elapsed_time(t1)
-
-    g_step = capture(step)
-    g_gemm = capture(gemm)
-    g_quant = capture(quant)
+    # Timed region: `steps` steps launched directly (a step of the headline
+    # workload is about a millisecond, so host launch cost is hidden), with a
+    # CUDA event before the quantiser, between the two kernels and after the
+    # GEMM, all on the launching stream, so that the kernel durations come
+    # from the timed region itself.
+    steps = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     with ClockSampler(local) as clk:
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
-        total_ms = timed(g_step, reps)
+        for i in range(steps):
+            ev[i][0].record(stream)
+            if c.has_quant:
+                c.quant(i)
+            ev[i][1].record(stream)
+            c.gemm(i)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-    # per-kernel durations: the same launches, one kernel kind per graph
-    gemm_ms = timed(g_gemm, reps)
-    quant_ms = timed(g_quant, reps)
+    total_ms = ev[0][0].elapsed_time(ev[steps - 1][2])
+    quant_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    gemm_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
     total_ms = max_over_ranks(total_ms, device=dev)
 
-    # end to end: pinned host activations in, bf16 result out, every step,
-    # through the public API with one launch per call.  Independent steps are
-    # pipelined over three streams (copy in, compute, copy out); a buffer set
-    # is reused only after its previous step's copy out has completed.
-    x_pin = torch.from_numpy(x_host).pin_memory()
-    d_pins = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(n_sets)]
-    ev_cmp = [torch.cuda.Event() for _ in range(n_sets)]
-    ev_out = [torch.cuda.Event() for _ in range(n_sets)]
-    used = [False] * n_sets
+    flops_step = c.flops
+    value = job_throughput(world, flops_step, steps, total_ms) / 1e12
 
-    def e2e_step(i):
-        j = i % n_sets
-        if used[j]:
-            s_in.wait_event(ev_out[j])
-        used[j] = True
-        with torch.cuda.stream(s_in):
-            xs[j].copy_(x_pin, non_blocking=True)
-        ev_in[j].record(s_in)
-        s_cmp.wait_event(ev_in[j])
-        dg.dg_quant_act_1x128(xs[j], qas[j], sfas[j], stream=s_cmp.cuda_stream)
-        dg.dg_fp8_gemm_nt(qas[j], sfas[j], qbs[j], sfbs[j], ds[j], stream=s_cmp.cuda_stream)
-        ev_cmp[j].record(s_cmp)
-        s_out.wait_event(ev_cmp[j])
-        with torch.cuda.stream(s_out):
-            d_pins[i % 2].copy_(ds[j], non_blocking=True)
-        ev_out[j].record(s_out)
-
-    for i in range(2 * n_sets):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_steps = min(args.steps, 500)
-    e0.record(s_in)
-    for i in range(e2e_steps):
-        e2e_step(i)
-    e1.record(s_out)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-
-    flops_step = 2.0 * M * N * K
-    value = job_throughput(world, flops_step, steps_run, total_ms) / 1e12
-    e2e_ms = max_over_ranks(e2e_ms, device=dev)
-    e2e_value = job_throughput(world, flops_step, e2e_steps, e2e_ms) / 1e12
-
-    hbm, bf16, bf16_sus, src = peaks()
-    fp8_peak = bf16 * FP8_PER_BF16
-    gemm_s = gemm_ms / steps_run * 1e-3
-    ab = algorithmic_bytes(w)
-    t_mem = ab / (hbm * 1e9)
-    t_cmp = flops_step / (fp8_peak * 1e12)
-    if t_mem >= t_cmp:
-        roof = {"bound": "hbm", "achieved": ab / gemm_s / 1e9, "peak": hbm, "unit": "GB/s"}
-    else:
-        roof = {"bound": "tensor", "achieved": flops_step / gemm_s / 1e12, "peak": fp8_peak, "unit": "TFLOP/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = measured_traffic(f"fp8_gemm_{w.name}_M{M}_N{N}_K{K}.md")
-    roof["peak_source"] = f"{src} (MEASURED_PEAKS.json; fp8 = bf16 x {FP8_PER_BF16:g})" if src == "measured" \
-        else "fallback"
+    roof = roofline(flops_step, c.bytes, gemm_ms * 1e-3, hbm, fp8_peak)
+    prof_name = f"fp8_gemm_{w.name}.md"
+    roof["traffic"] = measured_traffic(prof_name)
+    roof["peak_source"] = (f"{src} (MEASURED_PEAKS.json: bf16 burst {bf16:g} TFLOP/s x {FP8_PER_BF16:g} for fp8; "
+                           f"sustained {bf16_sus:g} x {FP8_PER_BF16:g} = {bf16_sus * FP8_PER_BF16:g}; "
+                           f"HBM {hbm:g} GB/s)" if src == "measured" else "fallback")
     roof["kernel"] = "fp8_gemm_kernel"
-    roof["kernel_us"] = gemm_s * 1e6
-    roof["quant_us"] = quant_ms / steps_run * 1e3
-    roof["algorithmic_bytes"] = ab
+    roof["kernel_us"] = gemm_ms * 1e3
+    roof["algorithmic_bytes"] = c.bytes
+    roof["useful_flop"] = flops_step
+    if c.has_quant:
+        qbytes = quant_bytes(c.rows, c.K)
+        roof["quant_us"] = quant_ms * 1e3
+        roof["quant_gbs"] = qbytes / (quant_ms * 1e-3) / 1e9
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps_run,
-        "warmup": args.warmup, "ms_per_step": total_ms / steps_run, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
-        "config": {"workload": describe(w), "l2": f"rotating {n_sets} input sets of {set_bytes / 1e6:.1f} MB "
-                                                  f"(> 2x L2) between steps",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic (seeded, random init)",
+        "config": {"workload": describe(w), "l2": c.l2_note(),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roof,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": M * K * 4, "d2h_bytes_per_step": M * N * 2},
-        "gpu_launches": 2 * steps_run,
-        "launch": f"CUDA graph of {chunk} steps replayed {reps} times; kernel times from graphs of the same "
-                  f"launches of one kernel",
+        "gpu_launches": (2 if c.has_quant else 1) * steps,
+        "launch": "direct launches on one stream with CUDA events around each kernel",
         "clocks": clk.summary(),
     }
+
+    if not args.no_e2e:
+        line["e2e"] = e2e(torch, dg, c, args, world, dev)
+
+    if rank == 0 and world == 1 and not args.no_extra:
+        configs = {}
+        for name in EXTRA:
+            if name == w.name:
+                continue
+            configs[name] = extra_config(torch, dg, name, dev, hbm, fp8_peak)
+        line["configs"] = configs
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, rows, el, thr = cpu_oracle_rate(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": thr, "kind": "oracle",
-                                "sample": f"oracle quantise + GEMM over {rows} rows of the {M}-row workload "
-                                          f"(row range repeated, {el:.1f} s of CPU time), rate in TFLOP/s"}
+                                "sample": f"oracle quantise + GEMM over {rows} useful rows of the {c.rows}-row "
+                                          f"workload (seeded permutation, chunks of up to 64 rows, "
+                                          f"{el:.1f} s of CPU time), rate in TFLOP/s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
-def main():
-    args = parse()
-    w = wl.WORKLOADS[args.workload]
+def e2e(torch, dg, c: Case, args, world: int, dev) -> dict:
+    """End to end through the public API: every step copies its fp32
+    activations (and the MoE metadata) from pinned host memory to the device,
+    runs the quantiser and the GEMM, and copies D back to pinned host memory.
+    Independent steps are pipelined over three streams (copy in, compute,
+    copy out) with two buffer sets; a set is reused only after its previous
+    copy out has completed."""
+    nbuf = 2
+    x_pin = torch.from_numpy(c.x_host).pin_memory()
+    meta_pin = None if c.meta is None else c.meta.cpu().pin_memory()
+    d_pins = [torch.empty(c.ds[0].shape, dtype=torch.bfloat16).pin_memory() for _ in range(nbuf)]
+    xs = [c.xs[0]] + [torch.empty_like(c.xs[0]) for _ in range(nbuf - 1)]
+    metas = None if c.meta is None else [torch.empty_like(c.meta) for _ in range(nbuf)]
+    qas = [c.qas[0]] + [torch.empty_like(c.qas[0]) for _ in range(nbuf - 1)]
+    sfas = [c.sfas[0]] + [torch.empty_like(c.sfas[0]) for _ in range(nbuf - 1)]
+    ds = [c.ds[0]] + [torch.empty_like(c.ds[0]) for _ in range(nbuf - 1)]
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_cmp = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_out = [torch.cuda.Event() for _ in range(nbuf)]
+    used = [False] * nbuf
+    w = c.w
+
+    def step(i):
+        j = i % nbuf
+        if used[j]:
+            s_in.wait_event(ev_out[j])
+        used[j] = True
+        with torch.cuda.stream(s_in):
+            xs[j].copy_(x_pin, non_blocking=True)
+            if metas is not None:
+                metas[j].copy_(meta_pin, non_blocking=True)
+        ev_in[j].record(s_in)
+        s_cmp.wait_event(ev_in[j])
+        sc = s_cmp.cuda_stream
+        if w.layout == "masked":
+            for e in range(c.G):
+                dg.dg_quant_act_1x128(xs[j][e], qas[j][e], sfas[j][e], stream=sc)
+            dg.dg_fp8_grouped_masked(qas[j], sfas[j], c.qb, c.sfb, metas[j], ds[j], expected_m=w.max_m // 2,
+                                     stream=sc)
+        else:
+            dg.dg_quant_act_1x128(xs[j], qas[j], sfas[j], stream=sc)
+            if w.layout == "dense":
+                dg.dg_fp8_gemm_nt(qas[j], sfas[j], c.qb, c.sfb, ds[j], stream=sc)
+            else:
+                dg.dg_fp8_grouped_contiguous(qas[j], sfas[j], c.qb, c.sfb, metas[j], ds[j], stream=sc)
+        ev_cmp[j].record(s_cmp)
+        s_out.wait_event(ev_cmp[j])
+        with torch.cuda.stream(s_out):
+            d_pins[j].copy_(ds[j], non_blocking=True)
+        ev_out[j].record(s_out)
+
+    for i in range(2 * nbuf):
+        step(i)
+    torch.cuda.synchronize()
+    n = max(args.steps, 4) if c.x_host.nbytes > 64 * 2 ** 20 else min(max(args.steps, 100), 500)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for i in range(n):
+        step(i)
+    e1.record(s_out)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), device=dev)
+    h2d = c.x_host.nbytes + (0 if c.meta is None else c.meta.numel() * 4)
+    d2h = c.ds[0].numel() * 2
+    return {"value": job_throughput(world, c.flops, n, ms) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n,
+            "how": "pinned host fp32 activations in, bf16 D out, every step, three streams"}
+
+
+def main(argv=None):
+    args = parse(argv)
+    w = with_tokens(wl.WORKLOADS[args.workload], args.tokens)
     if args.shape:
         M, N, K = (int(v) for v in args.shape.split(","))
         w = wl.Workload(f"shape_{M}x{N}x{K}", "dense", M=M, N=N, K=K, seed=5)

@@ -1,7 +1,10 @@
-"""The benchmark's reporting helpers, on the CPU: the algorithmic byte count
-of the roofline, the gate that keeps ncu traffic only for the captured build,
-and the clock summary that decides whether a run is kept."""
+"""The benchmark's reporting helpers, on the CPU: the algorithmic byte and
+FLOP counts of the roofline, the bound it picks, the gate that keeps ncu
+traffic only for the captured build, the clock summary that decides whether
+a run is kept, and the default workload of the bench line."""
 import os
+
+import pytest
 
 import bench
 import workloads as wl
@@ -51,3 +54,46 @@ def test_clock_summary_reports_median_and_active_reasons():
     assert c.summary()["reasons"] == ["hw_slowdown"]
     c.lines = []
     assert c.summary()["reasons"] == ["unavailable"]
+
+
+def test_useful_flops_exclude_padding_rows_and_masked_tails():
+    w = wl.WORKLOADS["contig"]
+    assert bench.useful_flops(w) == 2.0 * w.tokens * w.N * w.K
+    w = wl.WORKLOADS["masked"]
+    assert bench.useful_flops(w) == 2.0 * int(wl.masked_counts(w.G, w.max_m, w.seed).sum()) * w.N * w.K
+    w = wl.WORKLOADS["sweep_n7168_k18432"]
+    assert bench.useful_flops(w) == 2.0 * 4096 * 7168 * 18432
+
+
+def test_roofline_picks_the_slower_of_compute_and_bytes():
+    # the contiguous MoE GEMM is tensor-bound, the skinny and masked ones HBM-bound
+    hbm, fp8 = 6797.2, 3791.4
+    for name, bound in [("contig", "tensor"), ("sweep_n2112_k7168", "tensor"), ("skinny", "hbm"), ("masked", "hbm")]:
+        w = wl.WORKLOADS[name]
+        r = bench.roofline(bench.useful_flops(w), bench.algorithmic_bytes(w), 1e-3, hbm, fp8)
+        assert r["bound"] == bound, name
+        assert r["frac"] == pytest.approx(r["achieved"] / r["peak"])
+    r = bench.roofline(2e12, 1e6, 1e-3, hbm, fp8)
+    assert r["unit"] == "TFLOP/s" and r["achieved"] == pytest.approx(2000.0)
+    r = bench.roofline(1e6, 5e9, 1e-3, hbm, fp8)
+    assert r["unit"] == "GB/s" and r["achieved"] == pytest.approx(5000.0)
+
+
+def test_quantiser_bytes():
+    # fp32 in, one code byte out and one fp32 scale per 128 values
+    assert bench.quant_bytes(256, 2048) == 256 * 2048 * 5 + 256 * 16 * 4
+
+
+def test_default_bench_line_is_the_contiguous_moe_workload():
+    args = bench.parse([])
+    assert args.workload == "contig" and args.gpus == 1 and args.warmup >= 3
+    w = wl.WORKLOADS[args.workload]
+    assert (w.layout, w.G, w.tokens, w.N, w.K) == ("contiguous", 8, 32768, 4096, 7168)
+    # every other workload is measured in the same run
+    assert set(bench.EXTRA) | {"contig"} == set(wl.WORKLOADS)
+
+
+def test_reduced_token_count_is_a_profiling_variant_only():
+    w = bench.with_tokens(wl.WORKLOADS["contig"], 4096)
+    assert w.tokens == 4096 and w.name != "contig" and w.N == 4096 and w.K == 7168
+    assert bench.with_tokens(wl.WORKLOADS["skinny"], 4096) is wl.WORKLOADS["skinny"]
