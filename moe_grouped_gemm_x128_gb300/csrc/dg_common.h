@@ -34,6 +34,17 @@ dg_status_t encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, int r
                               const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
                               CUtensorMapSwizzle swizzle);
 
+// The 256 x 256 tiles computed by a CTA pair (dg_gemm_pair.cu).  The
+// contiguous layout's list of row pairs lives in shared memory, so the pair
+// kernel takes at most this many 128-row blocks.
+constexpr int kPairMaxRows = 1024;
+bool pair_plan_ok(int layout, int M, int N, int K, int G, int num_sms);
+int pair_smem_bytes();
+int pair_num_tiles(int layout, int M, int N, int G);
+dg_status_t launch_pair(int layout, const uint8_t *a, const float *sfa, const uint8_t *b, const float *sfb,
+                        uint16_t *d, const int32_t *meta, int M, int N, int K, int G, int num_tiles_hint, void *stream,
+                        const DeviceInfo &info);
+
 inline bool aligned16(const void *p)
 {
     return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;

@@ -45,8 +45,11 @@
 // in flight, the MMA thread drains its MMAs, TMEM is freed and the CTA exits.
 #include <stdlib.h>
 
+#include <algorithm>
+
 #include "dg_common.h"
 #include "dg_ptx.cuh"
+#include "dg_wait.cuh"
 
 namespace dg {
 namespace {
@@ -68,8 +71,6 @@ struct Roles {
 constexpr int kGroupM = 16;                // m-blocks per rasterisation band
 constexpr int kMaxBufs = 5;                // TMEM partial buffers at most (512 columns / BN)
 constexpr int kMaxMaskedGroups = 1024;     // G limit of the masked layout (tile prefix in smem)
-// Pipeline waits give up after this many SM cycles (about 2 s at 2 GHz).
-constexpr long long kWaitTimeoutCycles = 4000000000ll;
 
 template <int BN, int STAGES, int EPI_COLS, int KPS>
 struct SmemLayout {
@@ -115,53 +116,6 @@ struct TileInfo {
     int rows;      // rows of the tile that are inside the problem
     bool skip;
 };
-
-__device__ __forceinline__ void raise_status(unsigned int *status, unsigned int bit)
-{
-    atomicOr(status, bit);
-}
-
-// Slow path of wait_phase: poll until the phase completes, another role
-// aborts, or about kWaitTimeoutCycles SM cycles pass.  The clock and the
-// abort flag are looked at every 64 polls only: a timer read is far slower
-// than a barrier test (%globaltimer costs hundreds of cycles).
-__device__ __forceinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                                unsigned int *status)
-{
-    const long long t0 = clock64();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_test_wait(bar, parity))
-            return true;
-        if ((it & 63u) == 0) {
-            if (*abort_flag)
-                return false;
-            if (clock64() - t0 > kWaitTimeoutCycles) {
-                *abort_flag = 1;
-                raise_status(status, DG_DEVFLAG_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
-
-// Bounded wait for the phase of `bar` with the given parity, by one thread:
-// one inline test, then the out-of-line polling loop.
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                           unsigned int *status)
-{
-    if (mbar_test_wait(bar, parity))
-        return true;
-    return wait_phase_slow(bar, parity, abort_flag, status);
-}
-
-// Bounded wait used while shutting down after an abort (ignores the flag).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
-{
-    const long long t0 = clock64();
-    for (uint32_t it = 1; !mbar_test_wait(bar, parity); ++it)
-        if ((it & 63u) == 0 && clock64() - t0 > kWaitTimeoutCycles)
-            return;
-}
 
 template <int BN>
 struct Sched {
@@ -799,6 +753,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1) __maxnreg__(
 
 // ----------------------------------------------------------------- host side
 struct Plan {
+    int bm;       // 128, or 256 for the CTA-pair kernel
     int bn;
     int stages;
     int num_tiles;
@@ -830,10 +785,11 @@ constexpr TileCfg kCfg192{192, 4, 64, 1};
 
 int forced_bn()
 {
-    // DG_FORCE_BN=96|128|192 pins the tile width (tests and sweeps)
+    // DG_FORCE_BN=96|128|192 pins the tile width of the one-SM kernel, 256
+    // the CTA-pair kernel (where the layout has one)
     const char *e = getenv("DG_FORCE_BN");
     const int b = e ? atoi(e) : 0;
-    return (b == 96 || b == 128 || b == 192) ? b : 0;
+    return (b == 96 || b == 128 || b == 192 || b == 256) ? b : 0;
 }
 
 int smem_for(int bn)
@@ -845,11 +801,27 @@ int smem_for(int bn)
 
 Plan make_plan(int layout, int M, int N, int K, int G, int num_sms, bool qout = false)
 {
-    (void)K;
     Plan pl;
+    // The CTA-pair kernel (256 x 256 tiles on two SMs) for bf16 output when
+    // the problem fills at least one wave of pairs: it takes in 63 bytes per
+    // SM cycle at the FP8 tensor rate, which one SM's TMA can sustain, where
+    // the one-SM tiles need 94-128.
+    const int fb = qout ? 0 : forced_bn();
+    if (!qout && pair_plan_ok(layout, M, N, K, G, num_sms) &&
+        (fb == 256 || (fb == 0 && pair_num_tiles(layout, M, N, G) >= num_sms / 2))) {
+        pl.bm = 256;
+        pl.bn = 256;
+        pl.stages = 3;
+        pl.smem = pair_smem_bytes();
+        pl.num_tiles = pair_num_tiles(layout, M, N, G);
+        pl.grid = layout == DG_LAYOUT_DENSE ? 2 * std::min(num_sms / 2, std::max(1, pl.num_tiles)) : 2 * (num_sms / 2);
+        return pl;
+    }
+    (void)K;
+    pl.bm = kBM;
     const int mblk = layout == DG_LAYOUT_MASKED ? G * ceil_div(M, kBM) : ceil_div(M, kBM);
     // a re-quantised output needs each 128-column scale group inside one tile
-    int bn = qout ? 128 : forced_bn();
+    int bn = qout ? 128 : (fb == 256 ? 0 : fb);
     if (bn == 0) {
         if (static_cast<long long>(mblk) * ceil_div(N, 192) >= num_sms) {
             bn = 192;
@@ -900,6 +872,8 @@ dg_status_t launch(int layout, const uint8_t *a, const float *sfa, const uint8_t
         return st;
     const bool qmode = qout != nullptr;
     const Plan pl = make_plan(layout, M, N, K, G, info.sm_count, qmode);
+    if (pl.bm == 256)
+        return launch_pair(layout, a, sfa, b, sfb, d, meta, M, N, K, G, pl.num_tiles, stream, info);
     const int ldsfa = round_up(M, 4);
 
     // Tensor maps view each K-major operand as [..][rows][K/128][128 bytes]:
@@ -1083,7 +1057,7 @@ extern "C" dg_status_t dg_query_plan(int layout, int M, int N, int K, int G, int
         num_sms = info.sm_count;
     }
     const dg::Plan pl = dg::make_plan(layout, M, N, K, G, num_sms);
-    out->block_m = dg::kBM;
+    out->block_m = pl.bm;
     out->block_n = pl.bn;
     out->stages = pl.stages;
     out->num_tiles = pl.num_tiles;

@@ -14,20 +14,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t global_timer_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ uint32_t lane_id()
-{
-    uint32_t l;
-    asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
-    return l;
-}
-
 // ------------------------------------------------- dependent launches ---
 // Programmatic dependent launch: a kernel launched with the programmatic
 // stream-serialisation attribute may start before the previous kernel in the
@@ -74,19 +60,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
         : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // Non-blocking test of the phase with the given parity.  Waiting loops spin
 // on this rather than on try_wait: a thread suspended inside try_wait can
 // resume hundreds of cycles after the phase completes.
@@ -107,16 +80,6 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t c0,
-                                            int32_t c1)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-        : "memory");
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t c0,
@@ -197,6 +160,107 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
                  : "memory");
 }
 
+// ------------------------------------------------ CTA pairs (clusters of 2) ---
+// A pair of CTAs in a cluster of two shares one tcgen05 MMA of M = 256: each
+// CTA holds 128 rows of A and half of B's rows in its own shared memory at the
+// same offsets, and receives its 128 rows of D in its own tensor memory.  The
+// even CTA (rank 0) issues the MMAs; every tcgen05 instruction of such a kernel
+// uses .cta_group::2.
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of both CTAs: all shared-memory writes and mbarrier
+// initialisations before it are visible to the peer after it.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The shared::cluster address of the location at shared::cta address `a` in
+// the cluster's CTA of rank `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t a, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+
+// Arrive once on an mbarrier given by its shared::cluster address (which may
+// lie in the peer CTA).  Default semantics (release at CTA scope): the
+// arriving thread's tensor-memory loads have completed (tcgen05.wait::ld)
+// before it arrives, which is all the peer's MMA needs; a cluster-scope
+// release costs about a microsecond here.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster)
+{
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is signalled on an
+// mbarrier of either CTA of the pair (`bar` is a shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t c0,
+                                                 int32_t c1, int32_t c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t c0,
+                                                 int32_t c1, int32_t c2, int32_t c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+// TMEM allocation for a CTA pair: one warp of each CTA executes it; both get
+// the same columns.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem of both CTAs] (+)= A[256 rows, split over the pair] * B^T[N cols,
+// split over the pair], FP8 x FP8 -> FP32, issued by one thread of rank 0.
+template <bool ACCUMULATE>
+__device__ __forceinline__ void mma_f8f6f4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, 1, %4;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "n"(ACCUMULATE ? 1 : 0)
+        : "memory");
+}
+
+// Arrive once on the mbarrier at the same shared-memory offset in each CTA of
+// `cta_mask` when every tcgen05 operation this thread issued has completed.
+__device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(cta_mask)
+        : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp receives
 // lane (base_lane + i), columns [col, col + 32).  Asynchronous: the registers
 // are valid only after tmem_wait_ld32 on the same array.
@@ -250,20 +314,6 @@ __device__ __forceinline__ void tmem_wait_ld16(uint32_t (&r)[16])
                    "+r"(r[14]), "+r"(r[15])
                  :
                  : "memory");
-}
-
-// Re-balance the register file between warpgroups: every warp of a
-// warpgroup executes the same one.
-template <uint32_t N>
-__device__ __forceinline__ void regs_dec()
-{
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
-template <uint32_t N>
-__device__ __forceinline__ void regs_inc()
-{
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
@@ -348,20 +398,31 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
-// Named barrier `id` over `count` threads that also ANDs a predicate across
-// them (bar.red.and.pred): every participant gets the same answer.
-__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, bool v)
+// ----------------------------------------------- small asynchronous copies ---
+// 4 bytes global -> shared, without holding registers; src_bytes = 0 writes
+// zero (nothing is read).  Completion per thread through commit/wait groups.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t src_bytes)
 {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 q, %3, 0;\n\t"
-        "bar.red.and.pred p, %1, %2, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"(id), "r"(count), "r"(static_cast<uint32_t>(v))
-        : "memory");
-    return r != 0;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Waits until at most N of this thread's committed groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
 }
 
 // ------------------------------------------------------------- epilogue ---

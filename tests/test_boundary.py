@@ -136,10 +136,31 @@ def test_plan_width_override(monkeypatch):
     for bn in (96, 128, 192):
         monkeypatch.setenv("DG_FORCE_BN", str(bn))
         p = dg.dg_query_plan(dg.DG_LAYOUT_DENSE, 4096, 7168, 2048, 1, num_sms=152)
-        assert p["block_n"] == bn and p["num_tiles"] == 32 * -(-7168 // bn)
+        assert p["block_m"] == 128 and p["block_n"] == bn and p["num_tiles"] == 32 * -(-7168 // bn)
+    # 256: the CTA-pair kernel, 256 x 256 tiles on two SMs, an even grid
+    monkeypatch.setenv("DG_FORCE_BN", "256")
+    p = dg.dg_query_plan(dg.DG_LAYOUT_DENSE, 300, 520, 256, 1, num_sms=152)
+    assert (p["block_m"], p["block_n"], p["num_tiles"], p["grid"]) == (256, 256, 2 * 3, 12)
+    # the masked layout has no pair kernel: the one-SM plan stays
+    p = dg.dg_query_plan(dg.DG_LAYOUT_MASKED, 256, 7168, 2048, 16, num_sms=152)
+    assert p["block_m"] == 128
     monkeypatch.setenv("DG_FORCE_BN", "100")   # not a compiled width: ignored
     p = dg.dg_query_plan(dg.DG_LAYOUT_DENSE, 4096, 7168, 2048, 1, num_sms=152)
-    assert p["block_n"] == 192
+    assert (p["block_m"], p["block_n"]) == (256, 256)
+
+
+def test_plan_picks_pair_tiles_for_a_full_wave_of_pairs():
+    # a full wave of 256 x 256 pair tiles (76 pairs on 152 SMs) takes the
+    # CTA-pair kernel; fewer keep the one-SM tiles (e.g. the skinny M=256 case)
+    p = dg.dg_query_plan(dg.DG_LAYOUT_DENSE, 4096, 7168, 18432, 1, num_sms=152)
+    assert (p["block_m"], p["block_n"], p["num_tiles"], p["grid"]) == (256, 256, 16 * 28, 152)
+    p = dg.dg_query_plan(dg.DG_LAYOUT_DENSE, 256, 7168, 2048, 1, num_sms=152)
+    assert p["block_m"] == 128
+    p = dg.dg_query_plan(dg.DG_LAYOUT_CONTIGUOUS, 33152, 4096, 7168, 8, num_sms=152)
+    assert (p["block_m"], p["block_n"], p["grid"]) == (256, 256, 152)
+    # contiguous pair rows live in shared memory: at most 2048 blocks of 128 rows
+    p = dg.dg_query_plan(dg.DG_LAYOUT_CONTIGUOUS, 2049 * 128, 4096, 7168, 8, num_sms=152)
+    assert p["block_m"] == 128
 
 
 def test_plan_shapes():
@@ -147,7 +168,10 @@ def test_plan_shapes():
         p = dg.dg_query_plan(dg.DG_LAYOUT_DENSE, M, N, K, 1, num_sms=152)
         tiles = -(-M // p["block_m"]) * -(-N // p["block_n"])
         assert p["num_tiles"] == tiles
-        assert p["grid"] == min(tiles, 152)
+        if p["block_m"] == 256:
+            assert p["grid"] == 2 * min(tiles, 76)
+        else:
+            assert p["grid"] == min(tiles, 152)
         assert p["smem_bytes"] <= 232448
     # masked: fixed grid = SM count (the real tile count lives on the device)
     p = dg.dg_query_plan(dg.DG_LAYOUT_MASKED, 256, 7168, 2048, 16, num_sms=152)

@@ -21,10 +21,12 @@ def built():
     dg.dg_read_device_status()
 
 
-@pytest.fixture(params=[96, 128, 192], ids=["bn96", "bn128", "bn192"])
+@pytest.fixture(params=[96, 128, 192, 256], ids=["bn96", "bn128", "bn192", "pair256"])
 def tile_n(request, monkeypatch):
     """Runs the test with each compiled tile width (the plan's choice is
-    pinned through DG_FORCE_BN)."""
+    pinned through DG_FORCE_BN): 96, 128 and 192 on one SM, and the 256 x 256
+    tiles of the CTA-pair kernel (dense and contiguous layouts; the masked
+    layout keeps the one-SM plan)."""
     monkeypatch.setenv("DG_FORCE_BN", str(request.param))
     return request.param
 
@@ -139,7 +141,9 @@ def test_contiguous_random_tolerance(G, tokens, N, K, tile_n):
     assert np.all(out[~valid] == wl.SENTINEL_BF16)
 
 
-def test_contiguous_bad_expert_is_flagged():
+@pytest.mark.parametrize("force", ["", "256"], ids=["auto", "pair256"])
+def test_contiguous_bad_expert_is_flagged(force, monkeypatch):
+    monkeypatch.setenv("DG_FORCE_BN", force)
     a, sfa, b, sfb, mi = contiguous_case(2, 200, 128, 128, seed=3, exact=True)
     mi = mi.copy()
     mi[:128] = 5            # expert 5 does not exist (G = 2)
@@ -149,6 +153,36 @@ def test_contiguous_bad_expert_is_flagged():
     assert np.all(out[:128] == wl.SENTINEL_BF16)
     ref = oracle.grouped_contiguous(a, sfa, b, sfb, mi, d=np.full_like(out, wl.SENTINEL_BF16))
     np.testing.assert_array_equal(out, ref)
+
+
+@pytest.mark.parametrize("force", ["", "256"], ids=["auto", "pair256"])
+def test_contiguous_mixed_block_is_flagged_and_skipped(force, monkeypatch):
+    """A 128-row block whose rows name two experts: rows that disagree with
+    the block's first row are not written and the device flags the block."""
+    monkeypatch.setenv("DG_FORCE_BN", force)
+    a, sfa, b, sfb, mi = contiguous_case(3, 500, 256, 256, seed=8, exact=True)
+    mi = mi.copy()
+    first = int(np.flatnonzero(mi == 1)[0])
+    mi[first + 5] = 2                        # one row of expert 2 inside expert 1's block
+    out = gpu_contiguous(a, sfa, b, sfb, mi)
+    assert dg.dg_read_device_status() & dg.DG_DEVFLAG_MIXED_BLOCK
+    assert np.all(out[first + 5] == wl.SENTINEL_BF16)
+    keep = mi.copy()
+    keep[first + 5] = -1                     # the oracle's view: that row is left alone
+    ref = oracle.grouped_contiguous(a, sfa, b, sfb, keep, d=np.full_like(out, wl.SENTINEL_BF16))
+    np.testing.assert_array_equal(out, ref)
+
+
+@pytest.mark.parametrize("G,tokens,N,K", [(5, 1700, 264, 384), (1, 300, 512, 256), (6, 2600, 520, 128)])
+def test_contiguous_pair_rows_odd_blocks_and_padding(G, tokens, N, K, monkeypatch):
+    """CTA-pair tiles on experts with odd numbers of 128-row blocks (the last
+    block of such an expert is computed alone), N not a multiple of 256 and
+    an odd number of K blocks: exact inputs, bit for bit."""
+    monkeypatch.setenv("DG_FORCE_BN", "256")
+    a, sfa, b, sfb, mi = contiguous_case(G, tokens, N, K, seed=G * 7 + N, exact=True)
+    ref = np.full((a.shape[0], N), wl.SENTINEL_BF16, dtype=np.uint16)
+    ref = oracle.grouped_contiguous(a, sfa, b, sfb, mi, d=ref)
+    np.testing.assert_array_equal(gpu_contiguous(a, sfa, b, sfb, mi), ref)
 
 
 # ----------------------------------------------------------------- masked --
