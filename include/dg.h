@@ -139,8 +139,10 @@ dg_status_t dg_fp8_grouped_contiguous(const uint8_t *a, const float *sfa, const 
  *   sfb [G][ceil(N/128)][K/128], masked_m int32 [G] (device),
  *   d out bf16 [G][max_m][N]: rows >= masked_m[g] are never written.
  * masked_m[g] outside [0, max_m] is clamped and flagged.  expected_m is a
- * host hint of the typical masked_m (0 = unknown) used only to pick the tile
- * plan; it never changes results. */
+ * host hint of the typical masked_m (0 = unknown: every buffer full) used
+ * only to pick the tile width (the m-blocks an expert is expected to fill
+ * decide how many tiles a wave has); it never changes results and the launch
+ * stays the same whatever masked_m holds. */
 dg_status_t dg_fp8_grouped_masked(const uint8_t *a, const float *sfa, const uint8_t *b,
                                   const float *sfb, uint16_t *d, const int32_t *masked_m, int G,
                                   int max_m, int N, int K, int expected_m, void *stream);
@@ -171,15 +173,21 @@ dg_status_t dg_fp8_grouped_masked_q(const uint8_t *a, const float *sfa, const ui
                                     const float *sfb, uint8_t *q, float *sfo, const int32_t *masked_m,
                                     int G, int max_m, int N, int K, int expected_m, void *stream);
 
-/* Host-only: the tile plan the GEMM entry points would launch for this
- * problem on a GPU with `num_sms` SMs (num_sms <= 0: the current device's).
- * Makes no CUDA call when num_sms > 0.  For DG_LAYOUT_DENSE, M is the row
- * count; CONTIGUOUS: M = sum_M; MASKED: M = max_m.  Tiles are 128 x 192 when
- * the problem has at least one full wave of them; otherwise 128 x 128 or
- * 128 x 96, whichever leaves the busiest CTA the fewest operand bytes; the
- * environment variable DG_FORCE_BN=96|128|192 (read at every call) pins the
- * width.  Results do not depend on the tile width. */
-dg_status_t dg_query_plan(int layout, int M, int N, int K, int G, int num_sms, dg_plan_t *out);
+/* Host-only: the tile plan the bf16-output GEMM entry points would launch for
+ * this problem on a GPU with `num_sms` SMs (num_sms <= 0: the current
+ * device's).  Makes no CUDA call when num_sms > 0.  For DG_LAYOUT_DENSE, M is
+ * the row count; CONTIGUOUS: M = sum_M; MASKED: M = max_m, and expected_m the
+ * masked call's hint (0 = none; ignored by the other layouts; < 0 invalid).
+ * Dense and contiguous problems with at least 16 K blocks that fill a wave of
+ * CTA pairs take 256 x 256 tiles on pairs of SMs (block_m = 256; contiguous:
+ * at most 1024 blocks of 128 rows); otherwise tiles are 128 x 192 when the
+ * problem has at least one full wave of them, else 128 x 128 or 128 x 96,
+ * whichever leaves the busiest CTA the fewest operand bytes.  The
+ * environment variable DG_FORCE_BN=96|128|192|256 (read at every call) pins
+ * the width (256: the CTA-pair tiles, dense and contiguous only).  Results do
+ * not depend on the plan. */
+dg_status_t dg_query_plan(int layout, int M, int N, int K, int G, int expected_m, int num_sms,
+                          dg_plan_t *out);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *dg_status_string(dg_status_t status);
@@ -188,6 +196,17 @@ const char *dg_status_string(dg_status_t status);
  * *flags (host) and clears it.  Returns DG_ERR_DEVICE_TIMEOUT if the timeout
  * bit was set, DG_OK otherwise (other bits are reported through *flags). */
 dg_status_t dg_read_device_status(int *flags, void *stream);
+
+/* Diagnostic of the failure-detection path: every pipeline wait of the GEMM
+ * kernels is bounded.  Enqueues one small kernel whose single thread
+ * waits, with the same bounded wait the GEMM pipelines use, on an mbarrier
+ * that nothing ever arrives on.  The wait gives up after `limit_cycles` SM
+ * cycles (1000 <= limit_cycles <= 4e9, about 2 s; DG_ERR_INVALID_ARG
+ * otherwise), sets DG_DEVFLAG_TIMEOUT in the device status word and the
+ * kernel returns: the context stays usable, and the next
+ * dg_read_device_status on the stream returns DG_ERR_DEVICE_TIMEOUT.  No copy,
+ * MMA or tensor memory is involved. */
+dg_status_t dg_selftest_wait_timeout(long long limit_cycles, void *stream);
 
 #ifdef __cplusplus
 }

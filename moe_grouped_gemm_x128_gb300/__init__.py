@@ -53,6 +53,7 @@ EXPORTED = (
     "dg_query_plan",
     "dg_status_string",
     "dg_read_device_status",
+    "dg_selftest_wait_timeout",
 )
 
 
@@ -95,8 +96,9 @@ def load() -> ctypes.CDLL:
         "dg_fp8_gemm_nt_q": [P, P, P, P, P, P, I, I, I, P],
         "dg_fp8_grouped_contiguous_q": [P, P, P, P, P, P, P, I, I, I, I, P],
         "dg_fp8_grouped_masked_q": [P, P, P, P, P, P, P, I, I, I, I, I, P],
-        "dg_query_plan": [I, I, I, I, I, I, ctypes.POINTER(dg_plan_t)],
+        "dg_query_plan": [I, I, I, I, I, I, I, ctypes.POINTER(dg_plan_t)],
         "dg_read_device_status": [ctypes.POINTER(ctypes.c_int), P],
+        "dg_selftest_wait_timeout": [ctypes.c_longlong, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -389,10 +391,11 @@ def dg_fp8_grouped_masked_q(a, sfa, b, sfb, masked_m, q=None, sfo=None, expected
     return q, sfo
 
 
-def dg_query_plan(layout: int, M: int, N: int, K: int, G: int = 1, num_sms: int = 0) -> dict:
-    """Tile plan for a problem (host-only when num_sms > 0)."""
+def dg_query_plan(layout: int, M: int, N: int, K: int, G: int = 1, num_sms: int = 0, expected_m: int = 0) -> dict:
+    """Tile plan for a problem (host-only when num_sms > 0); expected_m is the
+    masked layout's hint."""
     out = dg_plan_t()
-    _check("dg_query_plan", load().dg_query_plan(layout, M, N, K, G, num_sms, ctypes.byref(out)))
+    _check("dg_query_plan", load().dg_query_plan(layout, M, N, K, G, expected_m, num_sms, ctypes.byref(out)))
     return {f: getattr(out, f) for f, _ in dg_plan_t._fields_}
 
 
@@ -403,3 +406,10 @@ def dg_read_device_status(stream=None) -> int:
     if st not in (DG_OK, DG_ERR_DEVICE_TIMEOUT):
         _check("dg_read_device_status", st)
     return flags.value
+
+
+def dg_selftest_wait_timeout(limit_cycles: int = 2_000_000, stream=None) -> None:
+    """Enqueue the bounded-wait diagnostic: a kernel waits on a barrier that
+    nothing arrives on and gives up after `limit_cycles` SM cycles, setting
+    DG_DEVFLAG_TIMEOUT (read it with dg_read_device_status)."""
+    _check("dg_selftest_wait_timeout", load().dg_selftest_wait_timeout(int(limit_cycles), _stream(stream)))

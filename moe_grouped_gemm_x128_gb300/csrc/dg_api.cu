@@ -3,6 +3,7 @@
 #include <mutex>
 
 #include "dg_common.h"
+#include "dg_wait.cuh"
 
 // Problems only the GPU can see (bad MoE metadata, pipeline timeouts) are
 // OR-ed into this word by the kernels; dg_read_device_status reads and clears
@@ -170,4 +171,42 @@ extern "C" dg_status_t dg_read_device_status(int *flags, void *stream)
         return DG_ERR_CUDA;
     *flags = static_cast<int>(host);
     return (host & DG_DEVFLAG_TIMEOUT) ? DG_ERR_DEVICE_TIMEOUT : DG_OK;
+}
+
+namespace dg {
+namespace {
+
+// One thread waits, with the GEMMs' bounded wait, on an mbarrier that nothing
+// arrives on: the wait gives up after `limit` SM cycles, raises the CTA's
+// abort flag and DG_DEVFLAG_TIMEOUT, and the kernel returns.  No copy, MMA or
+// tensor memory is in flight, so nothing needs draining.
+__global__ void __launch_bounds__(32) selftest_wait_timeout_kernel(long long limit, unsigned int *status)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t abort_word;
+    if (threadIdx.x != 0)
+        return;
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    fence_mbarrier_init();
+    abort_word = 0;
+    volatile uint32_t *abort_flag = &abort_word;
+    // phase 0 never completes (its single arrival never comes), so the wait
+    // returns false after `limit` cycles with DG_DEVFLAG_TIMEOUT raised
+    (void)wait_phase(b, 0, abort_flag, status, limit);
+}
+
+}  // namespace
+}  // namespace dg
+
+extern "C" dg_status_t dg_selftest_wait_timeout(long long limit_cycles, void *stream)
+{
+    if (limit_cycles < 1000 || limit_cycles > dg::kWaitTimeoutCycles)
+        return DG_ERR_INVALID_ARG;
+    dg::DeviceInfo info;
+    dg_status_t st = dg::current_device(&info);
+    if (st != DG_OK)
+        return st;
+    dg::selftest_wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_cycles, info.status_word);
+    return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }

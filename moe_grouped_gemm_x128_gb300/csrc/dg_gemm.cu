@@ -226,6 +226,10 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1) __maxnreg__(
     // issuers alternate stages, so slot s is always written by issuer s % 2 and
     // each thread waits only for its own slot's previous release
     static_assert(kBufs % kIssuers == 0, "each TMEM slot must belong to one issuer");
+    // the issuers test a stage's full barrier by parity only: waiting for the
+    // TMEM slot's previous release first guarantees that every fill up to
+    // (this use - STAGES) has been consumed only while slots <= stages
+    static_assert(STAGES >= kBufs, "full-barrier parity test needs TMEM slots <= ring stages");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -799,16 +803,17 @@ int smem_for(int bn)
                       : SmemLayout<128, kCfg128.stages, kCfg128.epi_cols, kCfg128.kps>::kAlloc;
 }
 
-Plan make_plan(int layout, int M, int N, int K, int G, int num_sms, bool qout = false)
+Plan make_plan(int layout, int M, int N, int K, int G, int num_sms, bool qout = false, int expected_m = 0)
 {
     Plan pl;
     // The CTA-pair kernel (256 x 256 tiles on two SMs) for bf16 output when
-    // the problem fills at least one wave of pairs: it takes in 63 bytes per
-    // SM cycle at the FP8 tensor rate, which one SM's TMA can sustain, where
-    // the one-SM tiles need 94-128.
+    // the problem fills at least one wave of pairs and K is long enough
+    // (at least 16 K blocks) to amortise a tile's ring fill and store: it
+    // takes in 63 bytes per SM cycle at the FP8 tensor rate, which one SM's
+    // TMA can sustain, where the one-SM tiles need 94-128.
     const int fb = qout ? 0 : forced_bn();
     if (!qout && pair_plan_ok(layout, M, N, K, G, num_sms) &&
-        (fb == 256 || (fb == 0 && pair_num_tiles(layout, M, N, G) >= num_sms / 2))) {
+        (fb == 256 || (fb == 0 && K >= 16 * kBK && pair_num_tiles(layout, M, N, G) >= num_sms / 2))) {
         pl.bm = 256;
         pl.bn = 256;
         pl.stages = 3;
@@ -819,7 +824,11 @@ Plan make_plan(int layout, int M, int N, int K, int G, int num_sms, bool qout = 
     }
     (void)K;
     pl.bm = kBM;
-    const int mblk = layout == DG_LAYOUT_MASKED ? G * ceil_div(M, kBM) : ceil_div(M, kBM);
+    // masked: the m-blocks the typical expert fills (expected_m, the caller's
+    // hint; 0 = every buffer full) decide the width; the grid is fixed and
+    // the kernel walks the real tile count
+    const int rows_g = (layout == DG_LAYOUT_MASKED && expected_m > 0) ? std::min(expected_m, M) : M;
+    const int mblk = layout == DG_LAYOUT_MASKED ? G * ceil_div(rows_g, kBM) : ceil_div(M, kBM);
     // a re-quantised output needs each 128-column scale group inside one tile
     int bn = qout ? 128 : (fb == 256 ? 0 : fb);
     if (bn == 0) {
@@ -841,7 +850,7 @@ Plan make_plan(int layout, int M, int N, int K, int G, int num_sms, bool qout = 
     pl.bn = bn;
     pl.stages = bn == 192 ? kCfg192.stages : bn == 96 ? kCfg96.stages : kCfg128.stages;
     pl.smem = smem_for(bn);
-    pl.num_tiles = mblk * ceil_div(N, bn);
+    pl.num_tiles = (layout == DG_LAYOUT_MASKED ? G * ceil_div(M, kBM) : mblk) * ceil_div(N, bn);
     if (layout == DG_LAYOUT_MASKED)
         pl.grid = num_sms;   // fixed: the real tile count is only known on the device
     else
@@ -864,14 +873,15 @@ dg_status_t check_common(const void *a, const void *sfa, const void *b, const vo
 }
 
 dg_status_t launch(int layout, const uint8_t *a, const float *sfa, const uint8_t *b, const float *sfb, uint16_t *d,
-                   uint8_t *qout, float *sfo, const int32_t *meta, int M, int N, int K, int G, void *stream)
+                   uint8_t *qout, float *sfo, const int32_t *meta, int M, int N, int K, int G, void *stream,
+                   int expected_m = 0)
 {
     DeviceInfo info;
     dg_status_t st = current_device(&info);
     if (st != DG_OK)
         return st;
     const bool qmode = qout != nullptr;
-    const Plan pl = make_plan(layout, M, N, K, G, info.sm_count, qmode);
+    const Plan pl = make_plan(layout, M, N, K, G, info.sm_count, qmode, expected_m);
     if (pl.bm == 256)
         return launch_pair(layout, a, sfa, b, sfb, d, meta, M, N, K, G, pl.num_tiles, stream, info);
     const int ldsfa = round_up(M, 4);
@@ -963,7 +973,6 @@ extern "C" dg_status_t dg_fp8_grouped_masked(const uint8_t *a, const float *sfa,
                                              const float *sfb, uint16_t *d, const int32_t *masked_m, int G,
                                              int max_m, int N, int K, int expected_m, void *stream)
 {
-    (void)expected_m;
     dg_status_t st = dg::check_common(a, sfa, b, sfb, d, max_m, N, K);
     if (st != DG_OK)
         return st;
@@ -973,7 +982,8 @@ extern "C" dg_status_t dg_fp8_grouped_masked(const uint8_t *a, const float *sfa,
         return DG_ERR_UNSUPPORTED_SHAPE;
     if (!dg::aligned16(masked_m))
         return DG_ERR_MISALIGNED;
-    return dg::launch(DG_LAYOUT_MASKED, a, sfa, b, sfb, d, nullptr, nullptr, masked_m, max_m, N, K, G, stream);
+    return dg::launch(DG_LAYOUT_MASKED, a, sfa, b, sfb, d, nullptr, nullptr, masked_m, max_m, N, K, G, stream,
+                      expected_m);
 }
 
 // ---------------------------------------- re-quantised output (E4M3 + 1x128)
@@ -1027,7 +1037,6 @@ extern "C" dg_status_t dg_fp8_grouped_masked_q(const uint8_t *a, const float *sf
                                                const float *sfb, uint8_t *q, float *sfo, const int32_t *masked_m,
                                                int G, int max_m, int N, int K, int expected_m, void *stream)
 {
-    (void)expected_m;
     dg_status_t st = dg::check_common(a, sfa, b, sfb, q, max_m, N, K);
     if (st == DG_OK)
         st = dg::check_qout(q, sfo, N);
@@ -1042,9 +1051,10 @@ extern "C" dg_status_t dg_fp8_grouped_masked_q(const uint8_t *a, const float *sf
     return dg::launch(DG_LAYOUT_MASKED, a, sfa, b, sfb, nullptr, q, sfo, masked_m, max_m, N, K, G, stream);
 }
 
-extern "C" dg_status_t dg_query_plan(int layout, int M, int N, int K, int G, int num_sms, dg_plan_t *out)
+extern "C" dg_status_t dg_query_plan(int layout, int M, int N, int K, int G, int expected_m, int num_sms,
+                                     dg_plan_t *out)
 {
-    if (!out || M <= 0 || N <= 0 || K <= 0 || G <= 0 ||
+    if (!out || M <= 0 || N <= 0 || K <= 0 || G <= 0 || expected_m < 0 ||
         (layout != DG_LAYOUT_DENSE && layout != DG_LAYOUT_CONTIGUOUS && layout != DG_LAYOUT_MASKED))
         return DG_ERR_INVALID_ARG;
     if (K % dg::kBK != 0 || N % 8 != 0)
@@ -1056,7 +1066,7 @@ extern "C" dg_status_t dg_query_plan(int layout, int M, int N, int K, int G, int
             return st;
         num_sms = info.sm_count;
     }
-    const dg::Plan pl = dg::make_plan(layout, M, N, K, G, num_sms);
+    const dg::Plan pl = dg::make_plan(layout, M, N, K, G, num_sms, false, expected_m);
     out->block_m = pl.bm;
     out->block_n = pl.bn;
     out->stages = pl.stages;

@@ -476,9 +476,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
 bool pair_plan_ok(int layout, int M, int N, int K, int G, int num_sms)
 {
-    (void)K;
     (void)G;
     (void)N;
+    (void)K;
     if (num_sms < 2)
         return false;
     if (layout == DG_LAYOUT_DENSE)

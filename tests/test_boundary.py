@@ -105,6 +105,12 @@ def test_read_status_validation(lib):
     assert lib.dg_read_device_status(None, None) == dg.DG_ERR_INVALID_ARG
 
 
+def test_selftest_limit_validation(lib):
+    # the limit is checked before anything touches the device
+    assert lib.dg_selftest_wait_timeout(999, None) == dg.DG_ERR_INVALID_ARG
+    assert lib.dg_selftest_wait_timeout(4000000001, None) == dg.DG_ERR_INVALID_ARG
+
+
 def golden_block_counts():
     """The pages' worked example (tests/golden/block_counts_m256_n7168.txt)."""
     path = os.path.join(os.path.dirname(__file__), "golden", "block_counts_m256_n7168.txt")
@@ -141,6 +147,9 @@ def test_plan_width_override(monkeypatch):
     monkeypatch.setenv("DG_FORCE_BN", "256")
     p = dg.dg_query_plan(dg.DG_LAYOUT_DENSE, 300, 520, 256, 1, num_sms=152)
     assert (p["block_m"], p["block_n"], p["num_tiles"], p["grid"]) == (256, 256, 2 * 3, 12)
+    # forced: short K too
+    p = dg.dg_query_plan(dg.DG_LAYOUT_DENSE, 4096, 24576, 1536, 1, num_sms=152)
+    assert p["block_m"] == 256
     # the masked layout has no pair kernel: the one-SM plan stays
     p = dg.dg_query_plan(dg.DG_LAYOUT_MASKED, 256, 7168, 2048, 16, num_sms=152)
     assert p["block_m"] == 128
@@ -156,11 +165,36 @@ def test_plan_picks_pair_tiles_for_a_full_wave_of_pairs():
     assert (p["block_m"], p["block_n"], p["num_tiles"], p["grid"]) == (256, 256, 16 * 28, 152)
     p = dg.dg_query_plan(dg.DG_LAYOUT_DENSE, 256, 7168, 2048, 1, num_sms=152)
     assert p["block_m"] == 128
+    # short K (fewer than 16 K blocks): the one-SM tiles amortise better
+    p = dg.dg_query_plan(dg.DG_LAYOUT_DENSE, 4096, 24576, 1536, 1, num_sms=152)
+    assert (p["block_m"], p["block_n"]) == (128, 192)
     p = dg.dg_query_plan(dg.DG_LAYOUT_CONTIGUOUS, 33152, 4096, 7168, 8, num_sms=152)
     assert (p["block_m"], p["block_n"], p["grid"]) == (256, 256, 152)
-    # contiguous pair rows live in shared memory: at most 2048 blocks of 128 rows
-    p = dg.dg_query_plan(dg.DG_LAYOUT_CONTIGUOUS, 2049 * 128, 4096, 7168, 8, num_sms=152)
+    # contiguous pair rows live in shared memory: at most 1024 blocks of 128 rows
+    p = dg.dg_query_plan(dg.DG_LAYOUT_CONTIGUOUS, 1025 * 128, 4096, 7168, 8, num_sms=152)
     assert p["block_m"] == 128
+    p = dg.dg_query_plan(dg.DG_LAYOUT_CONTIGUOUS, 1024 * 128, 4096, 7168, 8, num_sms=152)
+    assert p["block_m"] == 256
+
+
+def test_masked_plan_follows_expected_m():
+    # 4 experts with 512-row buffers, N = 4096: every buffer full makes 16
+    # m-blocks, 352 tiles of 128 x 192; a hint of 40 rows per expert leaves 4
+    # m-blocks, 88 such tiles on 152 SMs, so the plan narrows them to 128
+    # (128 tiles, one wave)
+    full = dg.dg_query_plan(dg.DG_LAYOUT_MASKED, 512, 4096, 2048, 4, num_sms=152)
+    assert full["block_n"] == 192
+    hint = dg.dg_query_plan(dg.DG_LAYOUT_MASKED, 512, 4096, 2048, 4, num_sms=152, expected_m=40)
+    assert hint["block_n"] == 128
+    # the grid and the tile bound stay those of full buffers (the kernel reads
+    # masked_m on the device), and the hint never exceeds max_m
+    assert hint["grid"] == 152 and hint["num_tiles"] == 4 * 4 * 32
+    assert dg.dg_query_plan(dg.DG_LAYOUT_MASKED, 512, 4096, 2048, 4, num_sms=152, expected_m=5000) == full
+    # the other layouts ignore the hint
+    assert dg.dg_query_plan(dg.DG_LAYOUT_DENSE, 4096, 7168, 2048, 1, num_sms=152, expected_m=7) == \
+        dg.dg_query_plan(dg.DG_LAYOUT_DENSE, 4096, 7168, 2048, 1, num_sms=152)
+    with pytest.raises(dg.DgError):
+        dg.dg_query_plan(dg.DG_LAYOUT_MASKED, 512, 7168, 2048, 4, num_sms=152, expected_m=-1)
 
 
 def test_plan_shapes():

@@ -113,3 +113,85 @@ def test_masked_full_size_graph_sampled():
         rows = wl.sample_rows(v, 6, w.seed + e, must=[0, v - 1])
         ref = oracle.gemm_nt(a[e], sfa[e], b[e], sfb[e], rows=rows)
         tolerance_check(bf16_bits_to_f32(out[e, rows]), bf16_bits_to_f32(ref[rows]), f"masked expert {e}")
+
+
+# --------------------------------------------------- exact, full shapes ----
+# Operands in {-2..2} with scales 2^[-3,0]: (K/128) * 128 * 2^2 * 2^6 < 2^24 up
+# to K = 18432, so every partial, product and fp32 sum is exact and the GPU
+# must match the oracle bit for bit at the workloads' full shapes, in the
+# plan the library picks for them (the launch the benchmark times).
+def exact_codes(g, shape):
+    from helpers import int_codes
+    return int_codes(wl.exact_operands(g, shape))
+
+
+@pytest.mark.parametrize("name", ["tiny", "skinny", "sweep_n7168_k18432", "sweep_n24576_k1536", "sweep_n2112_k7168"])
+def test_dense_full_size_exact_sampled(name):
+    w = wl.WORKLOADS[name]
+    g = np.random.default_rng(500 + w.seed)
+    a = exact_codes(g, (w.M, w.K))
+    b = exact_codes(g, (w.N, w.K))
+    sfa = np.zeros((w.K // QB, oracle.round_up(w.M, 4)), np.float32)
+    sfa[:, :w.M] = wl.exact_scales(g, (w.K // QB, w.M))
+    sfb = wl.exact_scales(g, (-(-w.N // QB), w.K // QB))
+    d = dg.dg_fp8_gemm_nt(dev(a), dev(sfa), dev(b), dev(sfb))
+    out = bits(d)
+    rows = wl.sample_rows(w.M, 24, w.seed, must=edge_rows(w.M))
+    ref = oracle.gemm_nt(a, sfa, b, sfb, rows=rows)
+    np.testing.assert_array_equal(out[rows], ref[rows])
+
+
+def test_contiguous_full_size_exact_sampled():
+    w = wl.WORKLOADS["contig"]
+    counts, m_indices, seg = wl.contiguous_routing(w.G, w.tokens, w.seed)
+    g = np.random.default_rng(600)
+    sum_M = len(m_indices)
+    a = exact_codes(g, (sum_M, w.K))
+    b = exact_codes(g, (w.G, w.N, w.K))
+    sfa = wl.exact_scales(g, (w.K // QB, sum_M))
+    sfb = wl.exact_scales(g, (w.G, -(-w.N // QB), w.K // QB))
+    sent = wl.SENTINEL_BF16
+    d = torch.full((sum_M, w.N), sent, dtype=torch.int16, device="cuda")
+    dg.dg_fp8_grouped_contiguous(dev(a), dev(sfa), dev(b), dev(sfb), dev(m_indices), d.view(torch.bfloat16))
+    out = bits(d.view(torch.bfloat16))
+    must = []
+    for e in range(w.G):
+        must += [int(seg[e]), int(seg[e] + counts[e] - 1), int(seg[e]) + 127, int(seg[e]) + 128]
+    rows = wl.sample_rows(sum_M, 24, w.seed, must=must)
+    ref = oracle.grouped_contiguous(a, sfa, b, sfb, m_indices, rows=rows, d=np.full((sum_M, w.N), sent, np.uint16))
+    np.testing.assert_array_equal(out[rows], ref[rows])
+    assert np.all(out[m_indices < 0] == sent)
+
+
+def test_masked_full_size_exact_graph():
+    w = wl.WORKLOADS["masked"]
+    masked_m = wl.masked_counts(w.G, w.max_m, w.seed)
+    g = np.random.default_rng(700)
+    ld = oracle.round_up(w.max_m, 4)
+    a = exact_codes(g, (w.G, w.max_m, w.K))
+    b = exact_codes(g, (w.G, w.N, w.K))
+    sfa = wl.exact_scales(g, (w.G, w.K // QB, ld))
+    sfb = wl.exact_scales(g, (w.G, -(-w.N // QB), w.K // QB))
+    ta, tsa, tb, tsb, mm = dev(a), dev(sfa), dev(b), dev(sfb), dev(masked_m)
+    sent = wl.SENTINEL_BF16
+    d = torch.full((w.G, w.max_m, w.N), sent, dtype=torch.int16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        dg.dg_fp8_grouped_masked(ta, tsa, tb, tsb, mm, d.view(torch.bfloat16), expected_m=w.max_m // 2)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        dg.dg_fp8_grouped_masked(ta, tsa, tb, tsb, mm, d.view(torch.bfloat16), expected_m=w.max_m // 2)
+    d.fill_(sent)
+    graph.replay()
+    out = bits(d.view(torch.bfloat16))
+    for e in range(w.G):
+        v = int(masked_m[e])
+        assert np.all(out[e, v:] == sent), f"expert {e} wrote rows beyond masked_m"
+        if v == 0:
+            continue
+        rows = wl.sample_rows(v, 4, w.seed + e, must=[0, v - 1])
+        ref = oracle.gemm_nt(a[e], sfa[e], b[e], sfb[e], rows=rows)
+        np.testing.assert_array_equal(out[e, rows], ref[rows])

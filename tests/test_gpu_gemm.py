@@ -242,6 +242,25 @@ def test_masked_random_tolerance(tile_n):
         assert np.all(out[e, v:] == wl.SENTINEL_BF16)
 
 
+def test_masked_expected_m_changes_the_plan_not_the_result():
+    """expected_m only picks the tile width: a hint that narrows the tiles
+    gives the same bits as no hint, on exact inputs equal to the oracle."""
+    G, max_m, N, K = 4, 512, 4096, 512
+    mm = [40, 0, 512, 17]
+    a, sfa, b, sfb, masked_m = masked_case(G, max_m, N, K, mm, seed=41, exact=True)
+    assert dg.dg_query_plan(dg.DG_LAYOUT_MASKED, max_m, N, K, G, expected_m=40)["block_n"] != \
+        dg.dg_query_plan(dg.DG_LAYOUT_MASKED, max_m, N, K, G)["block_n"]
+    outs = []
+    for hint in (0, 40):
+        d = sentinel_tensor((G, max_m, N))
+        dg.dg_fp8_grouped_masked(dev(a), dev(sfa), dev(b), dev(sfb), dev(masked_m), d.view(torch.bfloat16),
+                                 expected_m=hint)
+        outs.append(bits(d.view(torch.bfloat16)))
+    np.testing.assert_array_equal(outs[0], outs[1])
+    ref = oracle.grouped_masked(a, sfa, b, sfb, masked_m, d=np.full(outs[0].shape, wl.SENTINEL_BF16, np.uint16))
+    np.testing.assert_array_equal(outs[1], ref)
+
+
 def test_masked_clamps_and_flags_bad_counts():
     a, sfa, b, sfb, _ = masked_case(3, 64, 128, 128, [0, 0, 0], seed=4, exact=True)
     masked_m = np.array([-5, 70, 10], np.int32)
