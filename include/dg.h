@@ -173,6 +173,46 @@ dg_status_t dg_fp8_grouped_masked_q(const uint8_t *a, const float *sfa, const ui
                                     const float *sfb, uint8_t *q, float *sfo, const int32_t *masked_m,
                                     int G, int max_m, int N, int K, int expected_m, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Beyond per-group-scaled FP8: the two formats the 2kiu.com DeepGEMM tutorial
+ * names beside it.  Both keep the accumulator in tensor memory across all of
+ * K (no promotion on the CUDA cores), one SM per 128-row tile.
+ * ------------------------------------------------------------------------ */
+
+/* BF16 GEMM (2kiu.com tutorial 1 and 2.2: BF16 beside FP8 as a
+ * low-precision format):
+ *     D[m][n] = bf16_rn(sum_k A[m][k] * B[n][k])
+ * with bf16 operands and an fp32 accumulator (the tensor core's summation of
+ * the exact products; on integer-valued inputs whose sums stay exact in
+ * fp32 the result is unique).
+ *   a bf16 bits [M][K] (K-major), b bf16 bits [N][K] (K-major),
+ *   d out bf16 [M][N].
+ * K must be a multiple of 64 and N of 8 (DG_ERR_UNSUPPORTED_SHAPE). */
+dg_status_t dg_bf16_gemm_nt(const uint16_t *a, const uint16_t *b, uint16_t *d, int M, int N, int K,
+                            void *stream);
+
+/* MX (micro-scaling) quantiser (2kiu.com tutorial 7: MX formats with finer
+ * scale granularity; the format as the OCP Microscaling Formats (MX) v1.0
+ * specification defines it, with E4M3 elements): per row and 32-wide block
+ * of K values, e = floor(log2 amax) - 8 clamped to [-127, 127] (an all-zero
+ * block takes -127), scale code e + 127 (E8M0), codes E4M3 round-to-nearest-
+ * even with saturation of x * 2^-e (the block maximum lands in [256, 448]).
+ *   x fp32 [R][K]; q out E4M3 [R][K]; sx out E8M0 [R][K/32] (row-major).
+ * K must be a multiple of 128.  Bit-exact and deterministic. */
+dg_status_t dg_quant_mx_1x32(const float *x, uint8_t *q, uint8_t *sx, int R, int K, void *stream);
+
+/* MX GEMM (same sources): E4M3 operands with one E8M0 scale per 32
+ * consecutive K values of each row, applied per block by the tensor core
+ * (tcgen05.mma kind::mxf8f6f4, block scaling):
+ *     D[m][n] = bf16_rn(sum_kb 2^(sa[m][kb]-127) 2^(sb[n][kb]-127)
+ *                              sum_{k in block kb} dec(A[m][k]) dec(B[n][k]))
+ * with an fp32 accumulator.
+ *   a E4M3 [M][K], sa E8M0 [M][K/32], b E4M3 [N][K], sb E8M0 [N][K/32]
+ *   (the layouts dg_quant_mx_1x32 writes), d out bf16 [M][N].
+ * K must be a multiple of 128 and N of 8 (DG_ERR_UNSUPPORTED_SHAPE). */
+dg_status_t dg_mx_gemm_nt(const uint8_t *a, const uint8_t *sa, const uint8_t *b, const uint8_t *sb,
+                          uint16_t *d, int M, int N, int K, void *stream);
+
 /* Host-only: the tile plan the bf16-output GEMM entry points would launch for
  * this problem on a GPU with `num_sms` SMs (num_sms <= 0: the current
  * device's).  Makes no CUDA call when num_sms > 0.  For DG_LAYOUT_DENSE, M is

@@ -54,6 +54,9 @@ EXPORTED = (
     "dg_status_string",
     "dg_read_device_status",
     "dg_selftest_wait_timeout",
+    "dg_bf16_gemm_nt",
+    "dg_quant_mx_1x32",
+    "dg_mx_gemm_nt",
 )
 
 
@@ -99,6 +102,9 @@ def load() -> ctypes.CDLL:
         "dg_query_plan": [I, I, I, I, I, I, I, ctypes.POINTER(dg_plan_t)],
         "dg_read_device_status": [ctypes.POINTER(ctypes.c_int), P],
         "dg_selftest_wait_timeout": [ctypes.c_longlong, P],
+        "dg_bf16_gemm_nt": [P, P, P, I, I, I, P],
+        "dg_quant_mx_1x32": [P, P, P, I, I, P],
+        "dg_mx_gemm_nt": [P, P, P, P, P, I, I, I, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -413,3 +419,56 @@ def dg_selftest_wait_timeout(limit_cycles: int = 2_000_000, stream=None) -> None
     nothing arrives on and gives up after `limit_cycles` SM cycles, setting
     DG_DEVFLAG_TIMEOUT (read it with dg_read_device_status)."""
     _check("dg_selftest_wait_timeout", load().dg_selftest_wait_timeout(int(limit_cycles), _stream(stream)))
+
+
+# ------------------------------------------------------ BF16 and MX GEMMs --
+def dg_bf16_gemm_nt(a, b, d=None, stream=None):
+    """D = A . B^T on bf16 operands: a bf16 [M, K], b bf16 [N, K] -> bf16 [M, N]."""
+    import torch
+    T = _dtypes()
+    M, K = _dims(a, "a", 2)
+    N = _dims(b, "b", 2)[0]
+    if d is None:
+        d = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    _want(a, "a", (M, K), T["bf16"])
+    _want(b, "b", (N, K), T["bf16"])
+    _want(d, "d", (M, N), T["bf16"])
+    _on_device(("a", a), ("b", b), ("d", d))
+    _check("dg_bf16_gemm_nt", load().dg_bf16_gemm_nt(_ptr(a), _ptr(b), _ptr(d), M, N, K, _stream(stream)))
+    return d
+
+
+def dg_quant_mx_1x32(x, q=None, sx=None, stream=None):
+    """MX quantiser: x fp32 [R, K] -> (q uint8 E4M3 [R, K], sx uint8 E8M0 [R, K/32])."""
+    import torch
+    T = _dtypes()
+    R, K = _dims(x, "x", 2)
+    if q is None:
+        q = torch.empty((R, K), dtype=torch.uint8, device=x.device)
+    if sx is None:
+        sx = torch.empty((R, K // 32), dtype=torch.uint8, device=x.device)
+    _want(x, "x", (R, K), T["f32"])
+    _want(q, "q", (R, K), T["fp8"])
+    _want(sx, "sx", (R, K // 32), (torch.uint8,))
+    _on_device(("x", x), ("q", q), ("sx", sx))
+    _check("dg_quant_mx_1x32", load().dg_quant_mx_1x32(_ptr(x), _ptr(q), _ptr(sx), R, K, _stream(stream)))
+    return q, sx
+
+
+def dg_mx_gemm_nt(a, sa, b, sb, d=None, stream=None):
+    """MX GEMM: a E4M3 [M, K], sa E8M0 [M, K/32], b [N, K], sb [N, K/32] -> bf16 [M, N]."""
+    import torch
+    T = _dtypes()
+    M, K = _dims(a, "a", 2)
+    N = _dims(b, "b", 2)[0]
+    if d is None:
+        d = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    _want(a, "a", (M, K), T["fp8"])
+    _want(sa, "sa", (M, K // 32), (torch.uint8,))
+    _want(b, "b", (N, K), T["fp8"])
+    _want(sb, "sb", (N, K // 32), (torch.uint8,))
+    _want(d, "d", (M, N), T["bf16"])
+    _on_device(("a", a), ("sa", sa), ("b", b), ("sb", sb), ("d", d))
+    _check("dg_mx_gemm_nt", load().dg_mx_gemm_nt(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(d), M, N, K,
+                                                 _stream(stream)))
+    return d

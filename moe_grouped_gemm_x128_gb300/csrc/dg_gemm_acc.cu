@@ -1,0 +1,454 @@
+// GEMMs whose accumulator stays in tensor memory across all of K, for the two
+// formats the pages name beside per-group-scaled FP8 (2kiu.com DeepGEMM
+// tutorial, 1 and 2.2: BF16; 7: MX / micro-scaling formats with finer scale
+// granularity):
+//
+//   BF16   D = bf16_rn(sum_k A[m,k] B[n,k]) with bf16 operands
+//          (tcgen05.mma kind::f16, fp32 accumulator);
+//   MX     D = bf16_rn(sum_kb 2^(ea[m,kb] + eb[n,kb]) sum_{k in kb} A[m,k] B[n,k])
+//          with E4M3 operands and one UE8M0 scale per 32 consecutive K values
+//          of each row (OCP Microscaling v1.0), applied by the tensor core
+//          (tcgen05.mma kind::mxf8f6f4.block_scale.scale_vec::1X): the
+//          hardware scales every 32-wide block, so there is no promotion.
+//
+// One CTA per SM, persistent, 128 x BN tiles (BF16: 256 columns; MX: 128, so
+// that both scale matrices are one TMEM lane per row).  Roles:
+//   warp 0      TMA producer of A (one box of 128 rows x two 128-byte K
+//               chunks per stage; it also arms the stage's full barrier);
+//   warp 1      TMA producer of B (BN rows x two chunks);
+//   warp 2      allocates TMEM; lane 0 issues the MMAs of every stage into
+//               the tile's accumulator (one of two, alternating by tile),
+//               commits each stage to its "empty" barrier and the tile's last
+//               stage to the accumulator's "full" barrier;
+//   warps 4-7   (MX) scale writers: per stage and 128-wide K chunk, the
+//               scales of the tile's 128 rows of A and of B (one 32-bit word
+//               per row: the scales of the chunk's four 32-wide blocks) go
+//               into one 4-column TMEM granule each with tcgen05.st; the MMA
+//               of K step j selects byte j (the instruction's scale-factor ID);
+//   last 4 warps  epilogue: per tile, once the accumulator is complete, each
+//               thread loads its row 32 columns at a time, rounds to bf16 and
+//               stores through shared memory; the accumulator is released as
+//               soon as its TMEM loads are done, so the next tile's MMAs (into
+//               the other accumulator) overlap this tile's epilogue.
+// Every wait is bounded (dg_wait.cuh).
+#include <algorithm>
+
+#include "dg_common.h"
+#include "dg_ptx.cuh"
+#include "dg_wait.cuh"
+
+namespace dg {
+namespace {
+
+constexpr int kAccKind_BF16 = 0;
+constexpr int kAccKind_MX = 1;
+
+constexpr int kABM = 128;
+constexpr int kAKps = 2;                   // 128-byte K chunks per stage
+constexpr int kAGroupM = 16;               // m-blocks per rasterisation band
+
+template <int KIND>
+struct AccCfg {
+    static constexpr int kBN = KIND == kAccKind_BF16 ? 256 : 128;
+    static constexpr int kStages = KIND == kAccKind_BF16 ? 2 : 3;
+    static constexpr int kElemsPerChunk = KIND == kAccKind_BF16 ? 64 : 128;   // K values per 128-byte row
+    static constexpr int kSfWarps = KIND == kAccKind_MX ? 4 : 0;
+    static constexpr int kEpiWarp0 = 4 + kSfWarps;
+    static constexpr int kThreads = 32 * (kEpiWarp0 + 4);
+    static constexpr int kABox = kABM * 128 * kAKps;          // 32 KiB
+    static constexpr int kBBox = kBN * 128 * kAKps;           // 64 or 32 KiB
+    static constexpr int kAOff = 0;
+    static constexpr int kBOff = kAOff + kStages * kABox;
+    static constexpr int kOutRow = 32 * 2 + 16;               // 32 bf16 columns + 16 bytes of padding
+    static constexpr int kOutOff = kBOff + kStages * kBBox;
+    static constexpr int kBarOff = kOutOff + 4 * 32 * kOutRow;
+    // full[S], empty[S], sf_full[S], acc_full[2], acc_empty[2], drain
+    static constexpr int kMiscOff = kBarOff + 8 * (3 * kStages + 5);
+    static constexpr int kAlloc = kMiscOff + 16 + 1024;
+    // TMEM: two accumulators of kBN columns, then (MX) the scale columns of
+    // every stage: per chunk one column for A's scales and one for B's, each
+    // on its own 4-column (128-bit) boundary, the granule in which scale
+    // factors are laid out in tensor memory
+    static constexpr uint32_t kSfCol0 = 2 * kBN;
+    static constexpr uint32_t kSfStride = 8;                  // columns per chunk: A at +0, B at +4
+    static constexpr uint32_t kTmemCols = 512;
+    static_assert(kSfCol0 % 4 == 0 && kSfStride % 4 == 0, "scale columns on 4-column boundaries");
+    static_assert(2 * kBN + (KIND == kAccKind_MX ? kSfStride * kAKps * kStages : 0) <= 512, "TMEM columns");
+    static_assert(kAlloc <= 232448, "shared memory");
+};
+
+// Instruction descriptors (fp32 accumulator, both operands K-major):
+// kind::f16 with bf16 A and B (format 1 in bits 7-9 and 10-12), D format
+// f32 (1) in bits 4-5; kind::mxf8f6f4 with E4M3 A and B (format 0), UE8M0
+// scales (bit 23), the B and A scale-factor IDs (the byte of the scale word
+// that this K step uses) in bits 4-5 and 29-30.  N >> 3 in bits 17-22,
+// M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(uint32_t M, uint32_t N, uint32_t sf_id)
+{
+    return (sf_id << 4) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (sf_id << 29);
+}
+
+struct AccProblem {
+    int M;
+    int N;
+    int K;
+    int sf_ld;      // MX: scale bytes per row (K / 32)
+};
+
+template <int KIND>
+__global__ void __launch_bounds__(AccCfg<KIND>::kThreads, 1)
+    acc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                    const uint8_t *__restrict__ sfa, const uint8_t *__restrict__ sfb, uint16_t *__restrict__ d,
+                    AccProblem p, unsigned int *status)
+{
+    using C = AccCfg<KIND>;
+    constexpr int BN = C::kBN;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + C::kBarOff;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+    auto sf_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (3 * S + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (3 * S + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (3 * S + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + C::kMiscOff + 4);
+
+    const int pM = p.M, pN = p.N, pK = p.K, sf_ld = p.sf_ld;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int KC = pK / C::kElemsPerChunk;        // 128-byte K chunks
+    const int nst = (KC + kAKps - 1) / kAKps;     // stages per tile
+    const int m_blocks = (pM + kABM - 1) / kABM;
+    const int n_blocks = (pN + BN - 1) / BN;
+    const int num_tiles = m_blocks * n_blocks;
+    auto tile_mn = [m_blocks, n_blocks](int t, int &m0, int &n0) {
+        const int band_tiles = kAGroupM * n_blocks;
+        const int band = t / band_tiles;
+        const int first = band * kAGroupM;
+        const int band_m = min(m_blocks - first, kAGroupM);
+        const int local = t - band * band_tiles;
+        m0 = (first + local % band_m) * kABM;
+        n0 = (local / band_m) * BN;
+    };
+
+    // ------------------------------------------------------------------ setup
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+            mbar_init(sf_bar(s), 4);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 4);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&tmap_a);
+        tma_prefetch_desc(&tmap_b);
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    griddep_wait();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (threadIdx.x == 0)
+        griddep_launch_dependents();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp < 2) {
+        // ------------------------------------------------------- TMA producers
+        if (lane == 0) {
+            const bool is_a = warp == 0;
+            const CUtensorMap *map = is_a ? &tmap_a : &tmap_b;
+            const uint32_t dst0 = sbase + (is_a ? C::kAOff : C::kBOff);
+            const uint32_t box = is_a ? C::kABox : C::kBBox;
+            uint32_t gs = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+                int m0, n0;
+                tile_mn(t, m0, n0);
+                for (int j = 0; j < nst; ++j, ++gs) {
+                    const int s = static_cast<int>(gs % S);
+                    if (!wait_phase(empty_bar(s), ((gs / S) & 1u) ^ 1u, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (is_a)
+                        mbar_arrive_expect_tx(full_bar(s), C::kABox + C::kBBox);
+                    tma_load_3d(dst0 + s * box, map, full_bar(s), 0, is_a ? m0 : n0, j * kAKps);
+                }
+            }
+            if (!ok) {
+                // copies in flight complete on full barriers this thread may
+                // not observe; give them time to land before the CTA exits
+                const long long t0 = clock64();
+                while (clock64() - t0 < 20000000ll) {
+                }
+            }
+        }
+    } else if (warp == 2) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint64_t desc_a0 = smem_desc_sw128(sbase + C::kAOff);
+            const uint64_t desc_b0 = smem_desc_sw128(sbase + C::kBOff);
+            uint32_t gs = 0;
+            uint32_t tcount = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++tcount) {
+                const uint32_t buf = tcount & 1u;
+                // the epilogue has released this accumulator's previous tile
+                if (!wait_phase(acce_bar(buf), ((tcount >> 1) & 1u) ^ 1u, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * BN;
+                for (int j = 0; j < nst; ++j, ++gs) {
+                    const int s = static_cast<int>(gs % S);
+                    const uint32_t ph = (gs / S) & 1u;
+                    if (!wait_phase(full_bar(s), ph, abort_flag, status) ||
+                        (KIND == kAccKind_MX && !wait_phase(sf_bar(s), ph, abort_flag, status))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < kAKps; ++c) {
+                        const uint64_t da = desc_a0 + static_cast<uint64_t>((s * C::kABox + c * kABM * 128) >> 4);
+                        const uint64_t db = desc_b0 + static_cast<uint64_t>((s * C::kBBox + c * BN * 128) >> 4);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            // K step k of chunk c: 32 bytes further along the row;
+                            // the tile's first step overwrites the accumulator
+                            const uint32_t acc = (j > 0 || c > 0 || k > 0) ? 1u : 0u;
+                            if constexpr (KIND == kAccKind_BF16) {
+                                mma_f16(d_tmem, da + 2 * k, db + 2 * k, idesc_bf16_f32(kABM, BN), acc);
+                            } else {
+                                const uint32_t sf_col = tmem_base + C::kSfCol0 + C::kSfStride * (s * kAKps + c);
+                                mma_mx(d_tmem, da + 2 * k, db + 2 * k, idesc_mx_e4m3(kABM, BN, k), sf_col, sf_col + 4,
+                                       acc);
+                            }
+                        }
+                    }
+                    mma_commit(empty_bar(s));
+                }
+                if (!ok)
+                    break;
+                mma_commit(accf_bar(buf));
+            }
+            // every MMA this thread issued has completed once this barrier flips
+            mma_commit(drain_bar);
+            drain_wait(drain_bar, 0);
+        }
+    } else if (KIND == kAccKind_MX && warp >= 4 && warp < C::kEpiWarp0) {
+        // ------------------------------------------------------- scale writers
+        // Tensor-memory layout of one 128-wide K chunk's scales (for M or N =
+        // 128 rows, one scale per 32 K values): a 4-column (128-bit) granule
+        // in which lane l holds rows l, l + 32, l + 64 and l + 96 in columns
+        // 0-3, each 32-bit cell carrying the four scales of that row's four
+        // 32-wide blocks (byte j for K step j, the MMA's scale-factor ID),
+        // and every 32-lane quarter holds the same copy.  So each of the four
+        // warps writes the whole granule into its own quarter: thread l loads
+        // the four words of rows l + 32 i.  A stage's granules are rewritten
+        // only after its MMAs have completed (its empty barrier).
+        const int q = warp & 3;
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + C::kSfCol0;
+        uint32_t gs = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            int m0, n0;
+            tile_mn(t, m0, n0);
+            for (int j = 0; j < nst; ++j, ++gs) {
+                const int s = static_cast<int>(gs % S);
+                uint32_t got = 1;
+                if (lane == 0)
+                    got = wait_phase(empty_bar(s), ((gs / S) & 1u) ^ 1u, abort_flag, status) ? 1u : 0u;
+                if (__shfl_sync(0xffffffffu, got, 0) == 0) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < kAKps; ++c) {
+                    const int kc = j * kAKps + c;
+                    uint32_t wa[4], wb[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int ma = m0 + lane + 32 * i, nb = n0 + lane + 32 * i;
+                        wa[i] = (ma < pM && kc < KC)
+                                    ? __ldg(reinterpret_cast<const uint32_t *>(sfa + static_cast<size_t>(ma) * sf_ld) + kc)
+                                    : 0u;
+                        wb[i] = (nb < pN && kc < KC)
+                                    ? __ldg(reinterpret_cast<const uint32_t *>(sfb + static_cast<size_t>(nb) * sf_ld) + kc)
+                                    : 0u;
+                    }
+                    const uint32_t col = t_lane + C::kSfStride * (s * kAKps + c);
+                    tmem_st4(col, wa[0], wa[1], wa[2], wa[3]);
+                    tmem_st4(col + 4, wb[0], wb[1], wb[2], wb[3]);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                if (lane == 0)
+                    mbar_arrive(sf_bar(s));
+            }
+        }
+    } else if (warp >= C::kEpiWarp0) {
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        const uint32_t stage_u32 = sbase + C::kOutOff + q * 32 * C::kOutRow;
+        uint32_t tcount = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++tcount) {
+            int m0, n0;
+            tile_mn(t, m0, n0);
+            const uint32_t buf = tcount & 1u;
+            uint32_t got = 1;
+            if (lane == 0)
+                got = wait_phase(accf_bar(buf), (tcount >> 1) & 1u, abort_flag, status) ? 1u : 0u;
+            if (__shfl_sync(0xffffffffu, got, 0) == 0) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
+            const int rows_left = pM - (m0 + q * 32);
+            uint16_t *const d_warp = d + static_cast<size_t>(m0 + q * 32) * pN + n0;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(t_acc + c * 32, v);
+                tmem_wait_ld32(v);
+                if (c == BN / 32 - 1) {
+                    // the accumulator is free for the tile after next
+                    tc_fence_before();
+                    if (lane == 0)
+                        mbar_arrive(acce_bar(buf));
+                }
+                // this thread's row: 32 bf16 values = 64 bytes, staged so that
+                // the warp stores 8 rows x 64 bytes per instruction
+                const uint32_t my_row = stage_u32 + lane * C::kOutRow;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    st_shared_v4(my_row + 16 * k, pack_bf16x2(__uint_as_float(v[8 * k]), __uint_as_float(v[8 * k + 1])),
+                                 pack_bf16x2(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3])),
+                                 pack_bf16x2(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5])),
+                                 pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
+                __syncwarp();
+                const int cols_left = pN - (n0 + c * 32);
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const int rr = h * 8 + (lane >> 2);
+                    const int cc = lane & 3;
+                    if (rr < rows_left && cc * 8 < cols_left) {
+                        const uint4 w = ld_shared_v4(stage_u32 + rr * C::kOutRow + 16 * cc);
+                        st_global_v4(d_warp + static_cast<size_t>(rr) * pN + c * 32 + cc * 8, w.x, w.y, w.z, w.w);
+                    }
+                }
+                __syncwarp();
+            }
+        }
+    }
+
+    // ------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncwarp();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+template <int KIND>
+dg_status_t launch_acc(const void *a, const uint8_t *sfa, const void *b, const uint8_t *sfb, uint16_t *d, int M, int N,
+                       int K, void *stream)
+{
+    using C = AccCfg<KIND>;
+    DeviceInfo info;
+    dg_status_t st = current_device(&info);
+    if (st != DG_OK)
+        return st;
+    // operands viewed as [rows][K chunks][128 bytes]; a box is 128 bytes x
+    // rows x two chunks, 128-byte swizzled (the FP8 GEMM's layout)
+    const int esize = KIND == kAccKind_BF16 ? 2 : 1;
+    const CUtensorMapDataType dt = KIND == kAccKind_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const uint64_t inner = 128 / esize;
+    const uint64_t KC = static_cast<uint64_t>(K) / inner;
+    CUtensorMap ta, tb;
+    {
+        const uint64_t dims[3] = {inner, static_cast<uint64_t>(M), KC};
+        const uint64_t strides[2] = {static_cast<uint64_t>(K) * esize, 128};
+        const uint32_t box[3] = {static_cast<uint32_t>(inner), kABM, kAKps};
+        st = encode_tensor_map(&ta, dt, 3, a, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != DG_OK)
+            return st;
+    }
+    {
+        const uint64_t dims[3] = {inner, static_cast<uint64_t>(N), KC};
+        const uint64_t strides[2] = {static_cast<uint64_t>(K) * esize, 128};
+        const uint32_t box[3] = {static_cast<uint32_t>(inner), static_cast<uint32_t>(C::kBN), kAKps};
+        st = encode_tensor_map(&tb, dt, 3, b, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != DG_OK)
+            return st;
+    }
+    st = ensure_smem_attr(reinterpret_cast<const void *>(acc_gemm_kernel<KIND>), C::kAlloc);
+    if (st != DG_OK)
+        return st;
+    const int tiles = ceil_div(M, kABM) * ceil_div(N, C::kBN);
+    AccProblem prob{M, N, K, K / 32};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(std::min(tiles, info.sm_count));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kAlloc;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, acc_gemm_kernel<KIND>, ta, tb, sfa, sfb, d, prob, info.status_word) != cudaSuccess)
+        return DG_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace dg
+
+extern "C" dg_status_t dg_bf16_gemm_nt(const uint16_t *a, const uint16_t *b, uint16_t *d, int M, int N, int K,
+                                       void *stream)
+{
+    if (!a || !b || !d || M <= 0 || N <= 0 || K <= 0)
+        return DG_ERR_INVALID_ARG;
+    if (K % 64 != 0 || N % 8 != 0)
+        return DG_ERR_UNSUPPORTED_SHAPE;
+    if (!dg::aligned16(a) || !dg::aligned16(b) || !dg::aligned16(d))
+        return DG_ERR_MISALIGNED;
+    return dg::launch_acc<dg::kAccKind_BF16>(a, nullptr, b, nullptr, d, M, N, K, stream);
+}
+
+extern "C" dg_status_t dg_mx_gemm_nt(const uint8_t *a, const uint8_t *sa, const uint8_t *b, const uint8_t *sb,
+                                     uint16_t *d, int M, int N, int K, void *stream)
+{
+    if (!a || !sa || !b || !sb || !d || M <= 0 || N <= 0 || K <= 0)
+        return DG_ERR_INVALID_ARG;
+    if (K % 128 != 0 || N % 8 != 0)
+        return DG_ERR_UNSUPPORTED_SHAPE;
+    if (!dg::aligned16(a) || !dg::aligned16(sa) || !dg::aligned16(b) || !dg::aligned16(sb) || !dg::aligned16(d))
+        return DG_ERR_MISALIGNED;
+    return dg::launch_acc<dg::kAccKind_MX>(a, sa, b, sb, d, M, N, K, stream);
+}

@@ -152,6 +152,34 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uin
             : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T with bf16 operands (kind::f16), fp32
+// accumulator; `accumulate` = 0 overwrites D.  K = 16 values (32 bytes).
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= (A . 2^sfa) * (B . 2^sfb)^T, E4M3 operands with one UE8M0
+// scale per 32 K values of each row, applied by the tensor core
+// (kind::mxf8f6f4.block_scale.scale_vec::1X).  The scales are read from the
+// TMEM columns sfa_tmem / sfb_tmem (one lane per row), the byte given by the
+// instruction descriptor's scale-factor IDs.  K = 32 values.
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar)
@@ -292,6 +320,27 @@ __device__ __forceinline__ void tmem_wait_ld32(uint32_t (&r)[32])
                    "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
                  :
                  : "memory");
+}
+
+// One 32-bit column for the warp's 32 lanes: thread i writes lane
+// (base_lane + i) at column `taddr`.  Asynchronous until tmem_wait_st.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+// Four consecutive 32-bit columns for the warp's 32 lanes (thread i writes
+// lane base_lane + i, columns taddr .. taddr + 3).
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v0), "r"(v1),
+                 "r"(v2), "r"(v3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // 32 lanes x 16 consecutive 32-bit columns (same contract as tmem_ld32).

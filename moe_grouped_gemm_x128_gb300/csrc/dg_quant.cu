@@ -136,6 +136,42 @@ __global__ void __launch_bounds__(256) quant_weight_128x128_kernel(const float *
         sfb[(static_cast<size_t>(g) * NB + nb) * KB + kb] = s;
 }
 
+// MX quantiser (OCP Microscaling v1.0 with E4M3 elements): per row and
+// 32-wide block, e = floor(log2 amax) - 8 clamped to [-127, 127] (an all-zero
+// or subnormal block takes -127), scale code e + 127, codes E4M3 RNE with
+// saturation of x * 2^-e.  One warp quantises four blocks of one row (128
+// values, one 16-byte load per lane); the eight lanes of a block reduce its
+// amax with shuffles.  floor(log2 amax) is amax's exponent field; x * 2^-e
+// is one multiplication by a power of two, exact unless the product is
+// subnormal, where it is correctly rounded and then encodes to +-0.
+__global__ void __launch_bounds__(256) quant_mx_1x32_kernel(const float *__restrict__ x, uint8_t *__restrict__ q,
+                                                             uint8_t *__restrict__ sx, int R, int K)
+{
+    const int groups = K / 128;                   // 128-value groups per row
+    const long long tasks = static_cast<long long>(R) * groups;
+    const int lane = threadIdx.x & 31;
+    for (long long task = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5); task < tasks;
+         task += static_cast<long long>(gridDim.x) * 8) {
+        const int r = static_cast<int>(task / groups);
+        const int g = static_cast<int>(task % groups);
+        const size_t off = static_cast<size_t>(r) * K + static_cast<size_t>(g) * 128 + lane * 4;
+        const float4 v = __ldcs(reinterpret_cast<const float4 *>(x + off));
+        float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+        // lanes 8b..8b+7 hold block b of the group
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const int expo = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);   // 0 for zero / subnormal
+        int e = expo == 0 ? -127 : expo - 127 - 8;
+        e = e < -127 ? -127 : (e > 127 ? 127 : e);
+        const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);      // 2^-e, a normal float
+        const uint32_t packed = e4m3x4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+        __stcs(reinterpret_cast<uint32_t *>(q + off), packed);
+        if ((lane & 7) == 0)
+            sx[static_cast<size_t>(r) * (K / 32) + g * 4 + (lane >> 3)] = static_cast<uint8_t>(e + 127);
+    }
+}
+
 }  // namespace
 }  // namespace dg
 
@@ -200,5 +236,25 @@ extern "C" dg_status_t dg_quant_weight_128x128(const float *w, uint8_t *q, float
         return DG_ERR_UNSUPPORTED_SHAPE;
     quant_weight_128x128_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         w, q, sfb, N, K);
+    return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+}
+
+extern "C" dg_status_t dg_quant_mx_1x32(const float *x, uint8_t *q, uint8_t *sx, int R, int K, void *stream)
+{
+    using namespace dg;
+    if (!x || !q || !sx || R <= 0 || K <= 0)
+        return DG_ERR_INVALID_ARG;
+    if (K % 128 != 0)
+        return DG_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(sx))
+        return DG_ERR_MISALIGNED;
+    DeviceInfo info;
+    dg_status_t st = current_device(&info);
+    if (st != DG_OK)
+        return st;
+    const long long tasks = static_cast<long long>(R) * (K / 128);
+    const long long blocks = (tasks + 7) / 8;
+    const int grid = static_cast<int>(blocks < info.sm_count * 16LL ? blocks : info.sm_count * 16LL);
+    quant_mx_1x32_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, q, sx, R, K);
     return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }

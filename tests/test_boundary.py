@@ -101,6 +101,19 @@ def test_requant_gemm_validation(lib):
         dg.DG_ERR_UNSUPPORTED_SHAPE
 
 
+def test_bf16_and_mx_validation(lib):
+    F = FAKE
+    assert call(lib, "dg_bf16_gemm_nt", None, F, F, 128, 256, 64, None) == dg.DG_ERR_INVALID_ARG
+    assert call(lib, "dg_bf16_gemm_nt", F, F, F, 128, 256, 96, None) == dg.DG_ERR_UNSUPPORTED_SHAPE
+    assert call(lib, "dg_bf16_gemm_nt", F, F, F, 128, 252, 64, None) == dg.DG_ERR_UNSUPPORTED_SHAPE
+    assert call(lib, "dg_bf16_gemm_nt", F + 2, F, F, 128, 256, 64, None) == dg.DG_ERR_MISALIGNED
+    assert call(lib, "dg_quant_mx_1x32", F, F, None, 4, 128, None) == dg.DG_ERR_INVALID_ARG
+    assert call(lib, "dg_quant_mx_1x32", F, F, F, 4, 96, None) == dg.DG_ERR_UNSUPPORTED_SHAPE
+    assert call(lib, "dg_mx_gemm_nt", F, F, F, F, F, 128, 256, 192, None) == dg.DG_ERR_UNSUPPORTED_SHAPE
+    assert call(lib, "dg_mx_gemm_nt", F, F + 4, F, F, F, 128, 256, 256, None) == dg.DG_ERR_MISALIGNED
+    assert call(lib, "dg_mx_gemm_nt", F, F, F, F, F, 0, 256, 256, None) == dg.DG_ERR_INVALID_ARG
+
+
 def test_read_status_validation(lib):
     assert lib.dg_read_device_status(None, None) == dg.DG_ERR_INVALID_ARG
 
