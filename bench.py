@@ -482,6 +482,39 @@ def extra_config(torch, dg, name: str, dev, hbm: float, fp8_peak: float) -> dict
     return out
 
 
+NEXT_SHAPE = (4096, 7168, 7168)   # M, N, K of the BF16 and MX legs
+
+
+def next_format_legs(torch, dg, dev, bf16_peak: float, fp8_peak: float) -> dict:
+    """The two formats beside per-group-scaled FP8: a BF16 GEMM and an MX GEMM
+    (E4M3 with an E8M0 scale per 32 K values) at M=4096, N=7168, K=7168,
+    seeded N(0,1) inputs (MX: quantised by dg_quant_mx_1x32), timed as CUDA
+    graphs of repeated launches (inputs above L2)."""
+    M, N, K = NEXT_SHAPE
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    out = {}
+    flops = 2.0 * M * N * K
+    a32 = torch.randn((M, K), generator=g, device=dev)
+    b32 = torch.randn((N, K), generator=g, device=dev)
+    a16, b16 = a32.to(torch.bfloat16), b32.to(torch.bfloat16)
+    d = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ms = graph_time_ms(torch, lambda i: dg.dg_bf16_gemm_nt(a16, b16, d), 4, 10)
+    r = roofline(flops, (M * K + N * K + M * N) * 2, ms * 1e-3, 1e30, bf16_peak)
+    out["bf16"] = {"workload": f"BF16 GEMM M={M} N={N} K={K}", "kernel": "acc_gemm_kernel<bf16>", "kernel_us": ms * 1e3,
+                   "tflops": flops / (ms * 1e-3) / 1e12, **r, "peak_note": "measured bf16 burst peak"}
+    qa, sa = dg.dg_quant_mx_1x32(a32)
+    qb, sb = dg.dg_quant_mx_1x32(b32)
+    ms = graph_time_ms(torch, lambda i: dg.dg_mx_gemm_nt(qa, sa, qb, sb, d), 4, 10)
+    r = roofline(flops, M * K + N * K + (M + N) * K // 32 + M * N * 2, ms * 1e-3, 1e30, fp8_peak)
+    out["mx"] = {"workload": f"MX (E4M3, E8M0 per 32) GEMM M={M} N={N} K={K}", "kernel": "acc_gemm_kernel<mx>",
+                 "kernel_us": ms * 1e3, "tflops": flops / (ms * 1e-3) / 1e12, **r,
+                 "peak_note": "measured bf16 burst peak x 2 (FP8)"}
+    del a32, b32, a16, b16, qa, qb, d
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args, w):
     import torch
     import torch.distributed as dist
@@ -572,6 +605,7 @@ def run_gpu(args, w):
                 continue
             configs[name] = extra_config(torch, dg, name, dev, hbm, fp8_peak)
         line["configs"] = configs
+        line["next_formats"] = next_format_legs(torch, dg, dev, bf16, fp8_peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, rows, el, thr = cpu_oracle_rate(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": thr, "kind": "oracle",
