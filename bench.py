@@ -55,6 +55,8 @@ def parse(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile-next", default="", choices=["", "bf16", "mx"],
+                    help="run only the BF16 or MX GEMM leg a few times (profiling aid; not a bench line)")
     return ap.parse_args(argv)
 
 
@@ -194,7 +196,7 @@ def roofline(flops: float, nbytes: float, seconds: float, hbm: float, fp8_peak: 
 
 
 # -------------------------------------------------------- ncu traffic ------
-GEMM_SOURCES = ("dg_common.h", "dg_gemm.cu", "dg_ptx.cuh")
+GEMM_SOURCES = ("dg_common.h", "dg_gemm.cu", "dg_gemm_pair.cu", "dg_ptx.cuh", "dg_wait.cuh")
 
 
 def gemm_source_hash() -> str:
@@ -485,7 +487,7 @@ def extra_config(torch, dg, name: str, dev, hbm: float, fp8_peak: float) -> dict
 NEXT_SHAPE = (4096, 7168, 7168)   # M, N, K of the BF16 and MX legs
 
 
-def next_format_legs(torch, dg, dev, bf16_peak: float, fp8_peak: float) -> dict:
+def next_format_legs(torch, dg, dev, bf16_peak: float, fp8_peak: float, only: str = "") -> dict:
     """The two formats beside per-group-scaled FP8: a BF16 GEMM and an MX GEMM
     (E4M3 with an E8M0 scale per 32 K values) at M=4096, N=7168, K=7168,
     seeded N(0,1) inputs (MX: quantised by dg_quant_mx_1x32), timed as CUDA
@@ -497,20 +499,25 @@ def next_format_legs(torch, dg, dev, bf16_peak: float, fp8_peak: float) -> dict:
     flops = 2.0 * M * N * K
     a32 = torch.randn((M, K), generator=g, device=dev)
     b32 = torch.randn((N, K), generator=g, device=dev)
-    a16, b16 = a32.to(torch.bfloat16), b32.to(torch.bfloat16)
     d = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    ms = graph_time_ms(torch, lambda i: dg.dg_bf16_gemm_nt(a16, b16, d), 4, 10)
-    r = roofline(flops, (M * K + N * K + M * N) * 2, ms * 1e-3, 1e30, bf16_peak)
-    out["bf16"] = {"workload": f"BF16 GEMM M={M} N={N} K={K}", "kernel": "acc_gemm_kernel<bf16>", "kernel_us": ms * 1e3,
-                   "tflops": flops / (ms * 1e-3) / 1e12, **r, "peak_note": "measured bf16 burst peak"}
-    qa, sa = dg.dg_quant_mx_1x32(a32)
-    qb, sb = dg.dg_quant_mx_1x32(b32)
-    ms = graph_time_ms(torch, lambda i: dg.dg_mx_gemm_nt(qa, sa, qb, sb, d), 4, 10)
-    r = roofline(flops, M * K + N * K + (M + N) * K // 32 + M * N * 2, ms * 1e-3, 1e30, fp8_peak)
-    out["mx"] = {"workload": f"MX (E4M3, E8M0 per 32) GEMM M={M} N={N} K={K}", "kernel": "acc_gemm_kernel<mx>",
-                 "kernel_us": ms * 1e3, "tflops": flops / (ms * 1e-3) / 1e12, **r,
-                 "peak_note": "measured bf16 burst peak x 2 (FP8)"}
-    del a32, b32, a16, b16, qa, qb, d
+    if only in ("", "bf16"):
+        a16, b16 = a32.to(torch.bfloat16), b32.to(torch.bfloat16)
+        ms = graph_time_ms(torch, lambda i: dg.dg_bf16_gemm_nt(a16, b16, d), 4, 10)
+        r = roofline(flops, (M * K + N * K + M * N) * 2, ms * 1e-3, 1e30, bf16_peak)
+        out["bf16"] = {"workload": f"BF16 GEMM M={M} N={N} K={K}", "kernel": "acc_gemm_kernel<bf16>",
+                       "kernel_us": ms * 1e3, "tflops": flops / (ms * 1e-3) / 1e12, **r,
+                       "peak_note": "measured bf16 burst peak"}
+        del a16, b16
+    if only in ("", "mx"):
+        qa, sa = dg.dg_quant_mx_1x32(a32)
+        qb, sb = dg.dg_quant_mx_1x32(b32)
+        ms = graph_time_ms(torch, lambda i: dg.dg_mx_gemm_nt(qa, sa, qb, sb, d), 4, 10)
+        r = roofline(flops, M * K + N * K + (M + N) * K // 32 + M * N * 2, ms * 1e-3, 1e30, fp8_peak)
+        out["mx"] = {"workload": f"MX (E4M3, E8M0 per 32) GEMM M={M} N={N} K={K}", "kernel": "acc_gemm_kernel<mx>",
+                     "kernel_us": ms * 1e3, "tflops": flops / (ms * 1e-3) / 1e12, **r,
+                     "peak_note": "measured bf16 burst peak x 2 (FP8)"}
+        del qa, qb
+    del a32, b32, d
     torch.cuda.empty_cache()
     return out
 
@@ -688,8 +695,23 @@ def e2e(torch, dg, c: Case, args, world: int, dev) -> dict:
             "how": "pinned host fp32 activations in, bf16 D out, every step, three streams"}
 
 
+def profile_next(args):
+    import torch
+
+    import moe_grouped_gemm_x128_gb300 as dg
+    torch.cuda.set_device(0)
+    dg.build()
+    dg.load()
+    hbm, bf16, _, _ = peaks()
+    print(json.dumps(next_format_legs(torch, dg, torch.device("cuda", 0), bf16, bf16 * FP8_PER_BF16,
+                                      only=args.profile_next)), flush=True)
+
+
 def main(argv=None):
     args = parse(argv)
+    if args.profile_next:
+        profile_next(args)
+        return
     w = with_tokens(wl.WORKLOADS[args.workload], args.tokens)
     if args.shape:
         M, N, K = (int(v) for v in args.shape.split(","))
