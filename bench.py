@@ -401,6 +401,12 @@ class Case:
             self.ds.append(d)
         torch.cuda.synchronize()
 
+    def plan(self) -> dict:
+        w = self.w
+        return self.dg.dg_query_plan({"dense": 0, "contiguous": 1, "masked": 2}[w.layout],
+                                     w.max_m if w.layout == "masked" else self.rows, self.N, self.K, self.G,
+                                     expected_m=w.max_m // 2 if w.layout == "masked" else 0)
+
     @property
     def has_quant(self) -> bool:
         return self.w.layout != "masked"
@@ -430,6 +436,10 @@ class Case:
         if self.n_sets > 1:
             return f"rotating {self.n_sets} input sets of {self.set_bytes / 1e6:.1f} MB (> 2x L2) between launches"
         return f"inputs of {self.set_bytes / 1e6:.0f} MB per step (> 2x L2)"
+
+
+def gemm_kernel_name(plan: dict) -> str:
+    return "fp8_gemm_pair_kernel" if plan["block_m"] == 256 else "fp8_gemm_kernel"
 
 
 def graph_time_ms(torch, body, launches: int, reps: int) -> float:
@@ -466,10 +476,10 @@ def extra_config(torch, dg, name: str, dev, hbm: float, fp8_peak: float) -> dict
     torch.cuda.synchronize()
     gemm_ms = graph_time_ms(torch, c.gemm, launches, max(1, 200 // launches))
     r = roofline(c.flops, c.bytes, gemm_ms * 1e-3, hbm, fp8_peak)
-    out = {"workload": describe(w), "kernel": "fp8_gemm_kernel", "kernel_us": gemm_ms * 1e3,
+    plan = c.plan()
+    out = {"workload": describe(w), "kernel": gemm_kernel_name(plan), "kernel_us": gemm_ms * 1e3,
            "tflops": c.flops / (gemm_ms * 1e-3) / 1e12, "useful_flop": c.flops, "algorithmic_bytes": c.bytes, **r,
-           "plan": dg.dg_query_plan({"dense": 0, "contiguous": 1, "masked": 2}[w.layout],
-                                    w.max_m if w.layout == "masked" else c.rows, c.N, c.K, c.G),
+           "traffic": measured_traffic(f"fp8_gemm_{name}.md"), "plan": plan,
            "l2": c.l2_note(), "timing": f"CUDA graph of {launches} launches, replayed"}
     if w.layout == "masked":
         out["masked_m_sum"] = c.useful
@@ -581,7 +591,8 @@ def run_gpu(args, w):
     roof["peak_source"] = (f"{src} (MEASURED_PEAKS.json: bf16 burst {bf16:g} TFLOP/s x {FP8_PER_BF16:g} for fp8; "
                            f"sustained {bf16_sus:g} x {FP8_PER_BF16:g} = {bf16_sus * FP8_PER_BF16:g}; "
                            f"HBM {hbm:g} GB/s)" if src == "measured" else "fallback")
-    roof["kernel"] = "fp8_gemm_kernel"
+    roof["kernel"] = gemm_kernel_name(c.plan())
+    roof["plan"] = c.plan()
     roof["kernel_us"] = gemm_ms * 1e3
     roof["algorithmic_bytes"] = c.bytes
     roof["useful_flop"] = flops_step

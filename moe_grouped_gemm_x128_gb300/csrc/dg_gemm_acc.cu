@@ -268,44 +268,66 @@ __global__ void __launch_bounds__(AccCfg<KIND>::kThreads, 1)
         // only after its MMAs have completed (its empty barrier).
         const int q = warp & 3;
         const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + C::kSfCol0;
-        uint32_t gs = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-            int m0, n0;
-            tile_mn(t, m0, n0);
-            for (int j = 0; j < nst; ++j, ++gs) {
-                const int s = static_cast<int>(gs % S);
-                uint32_t got = 1;
-                if (lane == 0)
-                    got = wait_phase(empty_bar(s), ((gs / S) & 1u) ^ 1u, abort_flag, status) ? 1u : 0u;
-                if (__shfl_sync(0xffffffffu, got, 0) == 0) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < kAKps; ++c) {
-                    const int kc = j * kAKps + c;
-                    uint32_t wa[4], wb[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int ma = m0 + lane + 32 * i, nb = n0 + lane + 32 * i;
-                        wa[i] = (ma < pM && kc < KC)
-                                    ? __ldg(reinterpret_cast<const uint32_t *>(sfa + static_cast<size_t>(ma) * sf_ld) + kc)
-                                    : 0u;
-                        wb[i] = (nb < pN && kc < KC)
-                                    ? __ldg(reinterpret_cast<const uint32_t *>(sfb + static_cast<size_t>(nb) * sf_ld) + kc)
-                                    : 0u;
-                    }
-                    const uint32_t col = t_lane + C::kSfStride * (s * kAKps + c);
-                    tmem_st4(col, wa[0], wa[1], wa[2], wa[3]);
-                    tmem_st4(col + 4, wb[0], wb[1], wb[2], wb[3]);
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                if (lane == 0)
-                    mbar_arrive(sf_bar(s));
+        // The stages of all this CTA's tiles in order; the words of the next
+        // stage are loaded while the current one is written, into the other
+        // of two fixed register sets (the loop is unrolled by two, so no
+        // value moves between registers while its load is in flight).
+        const int total = ((num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                           static_cast<int>(gridDim.x)) * nst;
+        auto load_words = [&](int u, uint32_t (&w)[2 * kAKps][4]) {
+            if (u >= total) {
+                return;
             }
+            int m0, n0;
+            tile_mn(static_cast<int>(blockIdx.x) + (u / nst) * static_cast<int>(gridDim.x), m0, n0);
+            const int j = u % nst;
+#pragma unroll
+            for (int c = 0; c < kAKps; ++c) {
+                const int kc = j * kAKps + c;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int ma = m0 + lane + 32 * i, nb = n0 + lane + 32 * i;
+                    w[2 * c][i] = (ma < pM && kc < KC)
+                                      ? __ldg(reinterpret_cast<const uint32_t *>(sfa + static_cast<size_t>(ma) * sf_ld) + kc)
+                                      : 0u;
+                    w[2 * c + 1][i] = (nb < pN && kc < KC)
+                                          ? __ldg(reinterpret_cast<const uint32_t *>(sfb + static_cast<size_t>(nb) * sf_ld) + kc)
+                                          : 0u;
+                }
+            }
+        };
+        auto write_stage = [&](int u, uint32_t (&w)[2 * kAKps][4]) -> bool {
+            const uint32_t gs = static_cast<uint32_t>(u);
+            const int s = static_cast<int>(gs % S);
+            uint32_t got = 1;
+            if (lane == 0)
+                got = wait_phase(empty_bar(s), ((gs / S) & 1u) ^ 1u, abort_flag, status) ? 1u : 0u;
+            if (__shfl_sync(0xffffffffu, got, 0) == 0)
+                return false;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < kAKps; ++c) {
+                const uint32_t col = t_lane + C::kSfStride * (s * kAKps + c);
+                tmem_st4(col, w[2 * c][0], w[2 * c][1], w[2 * c][2], w[2 * c][3]);
+                tmem_st4(col + 4, w[2 * c + 1][0], w[2 * c + 1][1], w[2 * c + 1][2], w[2 * c + 1][3]);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            if (lane == 0)
+                mbar_arrive(sf_bar(s));
+            return true;
+        };
+        uint32_t w0[2 * kAKps][4], w1[2 * kAKps][4];
+        load_words(0, w0);
+        for (int u = 0; u < total; u += 2) {
+            load_words(u + 1, w1);
+            if (!write_stage(u, w0))
+                break;
+            if (u + 1 >= total)
+                break;
+            load_words(u + 2, w0);
+            if (!write_stage(u + 1, w1))
+                break;
         }
     } else if (warp >= C::kEpiWarp0) {
         // ---------------------------------------------------------- epilogue
