@@ -568,15 +568,12 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1) __maxnreg__(
                     const int jj = j % KPS;                       // K block within its ring stage
                     const bool last_of_slot = (jj == KPS - 1) || (kb == KB - 1);
                     if (jj == 0) {
-                        // wait until the MMAs of this stage are complete: lane 0
-                        // of each warp polls the barrier and shuffles the outcome
-                        // to its warp.  No bar.sync / bar.warp.sync here: those
-                        // order memory, which would make the scale loads issued
-                        // ahead complete first.
-                        uint32_t got = 1;
-                        if (lane == 0)
-                            got = wait_phase(tfull_bar(buf), tph, abort_flag, status) ? 1u : 0u;
-                        if (__shfl_sync(0xffffffffu, got, 0) == 0) {
+                        // wait until the MMAs of this stage are complete: every
+                        // lane polls (one test serves the warp; cheaper than one
+                        // poller and a broadcast).  No bar.sync / bar.warp.sync
+                        // here: those order memory, which would make the scale
+                        // loads issued ahead complete first.
+                        if (!__all_sync(0xffffffffu, wait_phase(tfull_bar(buf), tph, abort_flag, status))) {
                             ok = false;
                             break;
                         }

@@ -387,37 +387,44 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     // fp32 product of the two scales, rounded once
                     const float sc = ld_shared_f32(buf + (i * 32 + lane) * 4) * ld_shared_f32(buf + (64 + i) * 4);
                     const float2 s2 = make_float2(sc, sc);
-                    uint32_t got = 1;
-                    if (lane == 0)
-                        got = wait_phase(tfull_bar(i), gs & 1u, abort_flag, status) ? 1u : 0u;
-                    if (__shfl_sync(0xffffffffu, got, 0) == 0) {
+                    // every lane polls (the warp sees one result per test;
+                    // cheaper than one poller and a broadcast)
+                    if (!__all_sync(0xffffffffu, wait_phase(tfull_bar(i), gs & 1u, abort_flag, status))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t t_buf = t_lane + i * kPBN;
-                    // two 16-column loads in flight, then their FMAs
+                    // The slot is released once all four 16-column loads have
+                    // completed; the FMAs of the first two run while the last
+                    // two are in flight (a wait covers every load the thread
+                    // has issued, so the registers of a consumed chunk take
+                    // the next one).
+                    uint32_t v[16], w[16];
+                    tmem_ld16(t_buf, v);
+                    tmem_ld16(t_buf + 16, w);
+                    tmem_wait_ld16(v);
+                    tmem_wait_ld16(w);
 #pragma unroll
-                    for (int c = 0; c < kPEpiCols / 32; ++c) {
-                        uint32_t v[16], w[16];
-                        tmem_ld16(t_buf + c * 32, v);
-                        tmem_ld16(t_buf + c * 32 + 16, w);
-                        tmem_wait_ld16(v);
-                        tmem_wait_ld16(w);
-                        if (c == kPEpiCols / 32 - 1) {
-                            tc_fence_before();
-                            if (lane == 0)
-                                mbar_arrive_cluster(tempty0 + 8u * i);
-                        }
+                    for (int k = 0; k < 8; ++k)
+                        acc[k] = ffma2(make_float2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), s2, acc[k]);
+                    tmem_ld16(t_buf + 32, v);
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            acc[c * 16 + k] = ffma2(make_float2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])),
-                                                    s2, acc[c * 16 + k]);
+                    for (int k = 0; k < 8; ++k)
+                        acc[8 + k] =
+                            ffma2(make_float2(__uint_as_float(w[2 * k]), __uint_as_float(w[2 * k + 1])), s2, acc[8 + k]);
+                    tmem_ld16(t_buf + 48, w);
+                    tmem_wait_ld16(v);
+                    tmem_wait_ld16(w);
+                    tc_fence_before();
+                    if (lane == 0)
+                        mbar_arrive_cluster(tempty0 + 8u * i);
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            acc[c * 16 + 8 + k] =
-                                ffma2(make_float2(__uint_as_float(w[2 * k]), __uint_as_float(w[2 * k + 1])), s2,
-                                      acc[c * 16 + 8 + k]);
+                    for (int k = 0; k < 8; ++k) {
+                        acc[16 + k] =
+                            ffma2(make_float2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), s2, acc[16 + k]);
+                        acc[24 + k] =
+                            ffma2(make_float2(__uint_as_float(w[2 * k]), __uint_as_float(w[2 * k + 1])), s2, acc[24 + k]);
                     }
                 }
                 if (!ok)
