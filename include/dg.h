@@ -197,7 +197,13 @@ dg_status_t dg_bf16_gemm_nt(const uint16_t *a, const uint16_t *b, uint16_t *d, i
  * of K values, e = floor(log2 amax) - 8 clamped to [-127, 127] (an all-zero
  * block takes -127), scale code e + 127 (E8M0), codes E4M3 round-to-nearest-
  * even with saturation of x * 2^-e (the block maximum lands in [256, 448]).
- *   x fp32 [R][K]; q out E4M3 [R][K]; sx out E8M0 [R][K/32] (row-major).
+ *   x fp32 [R][K]; q out E4M3 [R][K];
+ *   sx out E8M0, chunk-major: [K/128][R] 32-bit words, the word of row r and
+ *   128-wide chunk g holding in byte j (little-endian) the scale code of the
+ *   row's 32-wide block 4 g + j.  (The row-major [R][K/32] codes, permuted so
+ *   that the GEMM reads one chunk's scales of consecutive rows as one
+ *   contiguous run, the order in which the tensor core takes them: four
+ *   scales per row per 128 K values.)
  * K must be a multiple of 128.  Bit-exact and deterministic. */
 dg_status_t dg_quant_mx_1x32(const float *x, uint8_t *q, uint8_t *sx, int R, int K, void *stream);
 
@@ -207,8 +213,9 @@ dg_status_t dg_quant_mx_1x32(const float *x, uint8_t *q, uint8_t *sx, int R, int
  *     D[m][n] = bf16_rn(sum_kb 2^(sa[m][kb]-127) 2^(sb[n][kb]-127)
  *                              sum_{k in block kb} dec(A[m][k]) dec(B[n][k]))
  * with an fp32 accumulator.
- *   a E4M3 [M][K], sa E8M0 [M][K/32], b E4M3 [N][K], sb E8M0 [N][K/32]
- *   (the layouts dg_quant_mx_1x32 writes), d out bf16 [M][N].
+ *   a E4M3 [M][K], b E4M3 [N][K]; sa, sb E8M0 scales in the chunk-major
+ *   layout dg_quant_mx_1x32 writes ([K/128][M] and [K/128][N] 32-bit words,
+ *   byte j of a word = block 4 g + j of chunk g); d out bf16 [M][N].
  * K must be a multiple of 128 and N of 8 (DG_ERR_UNSUPPORTED_SHAPE). */
 dg_status_t dg_mx_gemm_nt(const uint8_t *a, const uint8_t *sa, const uint8_t *b, const uint8_t *sb,
                           uint16_t *d, int M, int N, int K, void *stream);

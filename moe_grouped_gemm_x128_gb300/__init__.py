@@ -439,24 +439,28 @@ def dg_bf16_gemm_nt(a, b, d=None, stream=None):
 
 
 def dg_quant_mx_1x32(x, q=None, sx=None, stream=None):
-    """MX quantiser: x fp32 [R, K] -> (q uint8 E4M3 [R, K], sx uint8 E8M0 [R, K/32])."""
+    """MX quantiser: x fp32 [R, K] -> (q uint8 E4M3 [R, K], sx uint8 E8M0 [K/128, R, 4]).
+
+    sx is chunk-major: sx[g, r, j] is the scale code of row r's 32-wide block
+    4 g + j (the row-major [R, K/32] codes, permuted)."""
     import torch
     T = _dtypes()
     R, K = _dims(x, "x", 2)
     if q is None:
         q = torch.empty((R, K), dtype=torch.uint8, device=x.device)
     if sx is None:
-        sx = torch.empty((R, K // 32), dtype=torch.uint8, device=x.device)
+        sx = torch.empty((K // 128, R, 4), dtype=torch.uint8, device=x.device)
     _want(x, "x", (R, K), T["f32"])
     _want(q, "q", (R, K), T["fp8"])
-    _want(sx, "sx", (R, K // 32), (torch.uint8,))
+    _want(sx, "sx", (K // 128, R, 4), (torch.uint8,))
     _on_device(("x", x), ("q", q), ("sx", sx))
     _check("dg_quant_mx_1x32", load().dg_quant_mx_1x32(_ptr(x), _ptr(q), _ptr(sx), R, K, _stream(stream)))
     return q, sx
 
 
 def dg_mx_gemm_nt(a, sa, b, sb, d=None, stream=None):
-    """MX GEMM: a E4M3 [M, K], sa E8M0 [M, K/32], b [N, K], sb [N, K/32] -> bf16 [M, N]."""
+    """MX GEMM: a E4M3 [M, K], sa E8M0 [K/128, M, 4], b [N, K], sb [K/128, N, 4] -> bf16 [M, N]
+    (scales in the chunk-major layout dg_quant_mx_1x32 writes)."""
     import torch
     T = _dtypes()
     M, K = _dims(a, "a", 2)
@@ -464,9 +468,9 @@ def dg_mx_gemm_nt(a, sa, b, sb, d=None, stream=None):
     if d is None:
         d = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
     _want(a, "a", (M, K), T["fp8"])
-    _want(sa, "sa", (M, K // 32), (torch.uint8,))
+    _want(sa, "sa", (K // 128, M, 4), (torch.uint8,))
     _want(b, "b", (N, K), T["fp8"])
-    _want(sb, "sb", (N, K // 32), (torch.uint8,))
+    _want(sb, "sb", (K // 128, N, 4), (torch.uint8,))
     _want(d, "d", (M, N), T["bf16"])
     _on_device(("a", a), ("sa", sa), ("b", b), ("sb", sb), ("d", d))
     _check("dg_mx_gemm_nt", load().dg_mx_gemm_nt(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(d), M, N, K,

@@ -11,25 +11,32 @@
 //          (tcgen05.mma kind::mxf8f6f4.block_scale.scale_vec::1X): the
 //          hardware scales every 32-wide block, so there is no promotion.
 //
-// One CTA per SM, persistent, 128 x BN tiles (BF16: 256 columns; MX: 128, so
-// that both scale matrices are one TMEM lane per row).  Roles:
+// One CTA per SM, persistent, 128 x 256 tiles.  A K block of such a tile
+// brings 48 KB per 512 MMA cycles (one SM takes in at most ~80 bytes per cycle
+// through TMA), against 32 KB per 256 cycles for a 128 x 128 tile.  Roles:
 //   warp 0      TMA producer of A (one box of 128 rows x two 128-byte K
 //               chunks per stage; it also arms the stage's full barrier);
-//   warp 1      TMA producer of B (BN rows x two chunks);
+//   warp 1      TMA producer of B (256 rows x two chunks);
 //   warp 2      allocates TMEM; lane 0 issues the MMAs of every stage into
-//               the tile's accumulator (one of two, alternating by tile),
-//               commits each stage to its "empty" barrier and the tile's last
-//               stage to the accumulator's "full" barrier;
+//               the tile's accumulator, commits each stage to its "empty"
+//               barrier and the tile's last stage to the accumulator's "full"
+//               barrier.  BF16: one MMA of N = 256 per K step, two
+//               accumulators alternating by tile.  MX: two MMAs of N = 128 per
+//               K step (B rows 0-127 and 128-255, each with its own scale
+//               granule) into one accumulator: the scale columns take the
+//               room of the second;
 //   warps 4-7   (MX) scale writers: per stage and 128-wide K chunk, the
-//               scales of the tile's 128 rows of A and of B (one 32-bit word
-//               per row: the scales of the chunk's four 32-wide blocks) go
-//               into one 4-column TMEM granule each with tcgen05.st; the MMA
-//               of K step j selects byte j (the instruction's scale-factor ID);
-//   last 4 warps  epilogue: per tile, once the accumulator is complete, each
-//               thread loads its row 32 columns at a time, rounds to bf16 and
-//               stores through shared memory; the accumulator is released as
-//               soon as its TMEM loads are done, so the next tile's MMAs (into
-//               the other accumulator) overlap this tile's epilogue.
+//               scales of the tile's 128 rows of A and of each 128-row half
+//               of B (one 32-bit word per row: the scales of the chunk's four
+//               32-wide blocks) go into one 4-column TMEM granule each with
+//               tcgen05.st; the MMA of K step j selects byte j (the
+//               instruction's scale-factor ID).  They arrive on the stage's
+//               full barrier, so the issuer waits once per stage;
+//   epilogue    (BF16: 4 warps of 256 columns; MX: 8 warps of 128) per tile,
+//               once the accumulator is complete, each thread loads its row 32
+//               columns at a time, rounds to bf16 and stores through shared
+//               memory; the accumulator is released as soon as its TMEM loads
+//               are done.
 // Every wait is bounded (dg_wait.cuh).
 #include <algorithm>
 
@@ -49,31 +56,35 @@ constexpr int kAGroupM = 16;               // m-blocks per rasterisation band
 
 template <int KIND>
 struct AccCfg {
-    static constexpr int kBN = KIND == kAccKind_BF16 ? 256 : 128;
-    static constexpr int kStages = KIND == kAccKind_BF16 ? 2 : 3;
+    static constexpr int kBN = 256;
+    static constexpr int kStages = 2;
     static constexpr int kElemsPerChunk = KIND == kAccKind_BF16 ? 64 : 128;   // K values per 128-byte row
     static constexpr int kSfWarps = KIND == kAccKind_MX ? 4 : 0;
     static constexpr int kEpiWarp0 = 4 + kSfWarps;
-    static constexpr int kThreads = 32 * (kEpiWarp0 + 4);
+    static constexpr int kEpiWarps = KIND == kAccKind_MX ? 8 : 4;
+    static constexpr int kEpiCols = kBN / (kEpiWarps / 4);     // columns per epilogue warp
+    static constexpr int kAccBufs = KIND == kAccKind_MX ? 1 : 2;
+    static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
     static constexpr int kABox = kABM * 128 * kAKps;          // 32 KiB
-    static constexpr int kBBox = kBN * 128 * kAKps;           // 64 or 32 KiB
+    static constexpr int kBBox = kBN * 128 * kAKps;           // 64 KiB
     static constexpr int kAOff = 0;
     static constexpr int kBOff = kAOff + kStages * kABox;
     static constexpr int kOutRow = 32 * 2 + 16;               // 32 bf16 columns + 16 bytes of padding
     static constexpr int kOutOff = kBOff + kStages * kBBox;
-    static constexpr int kBarOff = kOutOff + 4 * 32 * kOutRow;
-    // full[S], empty[S], sf_full[S], acc_full[2], acc_empty[2], drain
-    static constexpr int kMiscOff = kBarOff + 8 * (3 * kStages + 5);
+    static constexpr int kBarOff = kOutOff + kEpiWarps * 32 * kOutRow;
+    // full[S], empty[S], acc_full[2], acc_empty[2], drain
+    static constexpr int kMiscOff = kBarOff + 8 * (2 * kStages + 5);
     static constexpr int kAlloc = kMiscOff + 16 + 1024;
-    // TMEM: two accumulators of kBN columns, then (MX) the scale columns of
-    // every stage: per chunk one column for A's scales and one for B's, each
-    // on its own 4-column (128-bit) boundary, the granule in which scale
-    // factors are laid out in tensor memory
-    static constexpr uint32_t kSfCol0 = 2 * kBN;
-    static constexpr uint32_t kSfStride = 8;                  // columns per chunk: A at +0, B at +4
+    // TMEM: the accumulators (kBN columns each), then (MX) the scale columns
+    // of every stage: per chunk one granule for A's scales and one for each
+    // 128-row half of B's, each on its own 4-column (128-bit) boundary, the
+    // granule in which scale factors are laid out in tensor memory
+    static constexpr uint32_t kSfCol0 = kAccBufs * kBN;
+    static constexpr uint32_t kSfStride = 12;                 // columns per chunk: A at +0, B halves at +4, +8
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kSfCol0 % 4 == 0 && kSfStride % 4 == 0, "scale columns on 4-column boundaries");
-    static_assert(2 * kBN + (KIND == kAccKind_MX ? kSfStride * kAKps * kStages : 0) <= 512, "TMEM columns");
+    static_assert(kAccBufs * kBN + (KIND == kAccKind_MX ? kSfStride * kAKps * kStages : 0) <= 512, "TMEM columns");
+    static_assert(kEpiWarps % 4 == 0 && kEpiCols % 32 == 0, "epilogue split");
     static_assert(kAlloc <= 232448, "shared memory");
 };
 
@@ -97,7 +108,6 @@ struct AccProblem {
     int M;
     int N;
     int K;
-    int sf_ld;      // MX: scale bytes per row (K / 32)
 };
 
 template <int KIND>
@@ -115,14 +125,14 @@ __global__ void __launch_bounds__(AccCfg<KIND>::kThreads, 1)
     const uint32_t bar0 = sbase + C::kBarOff;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
-    auto sf_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
-    auto accf_bar = [&](int b) { return bar0 + 8u * (3 * S + b); };
-    auto acce_bar = [&](int b) { return bar0 + 8u * (3 * S + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (3 * S + 4);
+    auto accf_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+    constexpr uint32_t kAB = C::kAccBufs;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + C::kMiscOff + 4);
 
-    const int pM = p.M, pN = p.N, pK = p.K, sf_ld = p.sf_ld;
+    const int pM = p.M, pN = p.N, pK = p.K;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int KC = pK / C::kElemsPerChunk;        // 128-byte K chunks
@@ -143,13 +153,14 @@ __global__ void __launch_bounds__(AccCfg<KIND>::kThreads, 1)
     // ------------------------------------------------------------------ setup
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full_bar(s), 1);
+            // the A producer's arrive (with the stage's bytes) and, for MX,
+            // one arrive per scale-writer warp
+            mbar_init(full_bar(s), 1 + C::kSfWarps);
             mbar_init(empty_bar(s), 1);
-            mbar_init(sf_bar(s), 4);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), 4);
+            mbar_init(acce_bar(b), C::kEpiWarps);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -210,9 +221,9 @@ __global__ void __launch_bounds__(AccCfg<KIND>::kThreads, 1)
             uint32_t tcount = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++tcount) {
-                const uint32_t buf = tcount & 1u;
+                const uint32_t buf = tcount % kAB;
                 // the epilogue has released this accumulator's previous tile
-                if (!wait_phase(acce_bar(buf), ((tcount >> 1) & 1u) ^ 1u, abort_flag, status)) {
+                if (!wait_phase(acce_bar(buf), ((tcount / kAB) & 1u) ^ 1u, abort_flag, status)) {
                     ok = false;
                     break;
                 }
@@ -221,8 +232,7 @@ __global__ void __launch_bounds__(AccCfg<KIND>::kThreads, 1)
                 for (int j = 0; j < nst; ++j, ++gs) {
                     const int s = static_cast<int>(gs % S);
                     const uint32_t ph = (gs / S) & 1u;
-                    if (!wait_phase(full_bar(s), ph, abort_flag, status) ||
-                        (KIND == kAccKind_MX && !wait_phase(sf_bar(s), ph, abort_flag, status))) {
+                    if (!wait_phase(full_bar(s), ph, abort_flag, status)) {
                         ok = false;
                         break;
                     }
@@ -239,9 +249,14 @@ __global__ void __launch_bounds__(AccCfg<KIND>::kThreads, 1)
                             if constexpr (KIND == kAccKind_BF16) {
                                 mma_f16(d_tmem, da + 2 * k, db + 2 * k, idesc_bf16_f32(kABM, BN), acc);
                             } else {
+                                // two MMAs of N = 128: B rows 0-127 into columns
+                                // 0-127, rows 128-255 into 128-255
                                 const uint32_t sf_col = tmem_base + C::kSfCol0 + C::kSfStride * (s * kAKps + c);
-                                mma_mx(d_tmem, da + 2 * k, db + 2 * k, idesc_mx_e4m3(kABM, BN, k), sf_col, sf_col + 4,
+                                constexpr uint64_t kHalfB = (128 * 128) >> 4;
+                                mma_mx(d_tmem, da + 2 * k, db + 2 * k, idesc_mx_e4m3(kABM, 128, k), sf_col, sf_col + 4,
                                        acc);
+                                mma_mx(d_tmem + 128, da + 2 * k, db + kHalfB + 2 * k, idesc_mx_e4m3(kABM, 128, k), sf_col,
+                                       sf_col + 8, acc);
                             }
                         }
                     }
@@ -257,15 +272,16 @@ __global__ void __launch_bounds__(AccCfg<KIND>::kThreads, 1)
         }
     } else if (KIND == kAccKind_MX && warp >= 4 && warp < C::kEpiWarp0) {
         // ------------------------------------------------------- scale writers
-        // Tensor-memory layout of one 128-wide K chunk's scales (for M or N =
-        // 128 rows, one scale per 32 K values): a 4-column (128-bit) granule
-        // in which lane l holds rows l, l + 32, l + 64 and l + 96 in columns
-        // 0-3, each 32-bit cell carrying the four scales of that row's four
-        // 32-wide blocks (byte j for K step j, the MMA's scale-factor ID),
-        // and every 32-lane quarter holds the same copy.  So each of the four
-        // warps writes the whole granule into its own quarter: thread l loads
-        // the four words of rows l + 32 i.  A stage's granules are rewritten
-        // only after its MMAs have completed (its empty barrier).
+        // Tensor-memory layout of one 128-wide K chunk's scales for 128 rows
+        // (one scale per 32 K values): a 4-column (128-bit) granule in which
+        // lane l holds rows l, l + 32, l + 64 and l + 96 in columns 0-3, each
+        // 32-bit cell carrying the four scales of that row's four 32-wide
+        // blocks (byte j for K step j, the MMA's scale-factor ID), and every
+        // 32-lane quarter holds the same copy.  So each of the four warps
+        // writes the whole granules into its own quarter: thread l loads the
+        // words of rows l + 32 i (A: 4 rows; B: 8, two granules).  A stage's
+        // granules are rewritten only after its MMAs have completed (its
+        // empty barrier).
         const int q = warp & 3;
         const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + C::kSfCol0;
         // The stages of all this CTA's tiles in order; the words of the next
@@ -274,7 +290,7 @@ __global__ void __launch_bounds__(AccCfg<KIND>::kThreads, 1)
         // value moves between registers while its load is in flight).
         const int total = ((num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                            static_cast<int>(gridDim.x)) * nst;
-        auto load_words = [&](int u, uint32_t (&w)[2 * kAKps][4]) {
+        auto load_words = [&](int u, uint32_t (&w)[kAKps][12]) {
             if (u >= total) {
                 return;
             }
@@ -286,38 +302,40 @@ __global__ void __launch_bounds__(AccCfg<KIND>::kThreads, 1)
                 const int kc = j * kAKps + c;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int ma = m0 + lane + 32 * i, nb = n0 + lane + 32 * i;
-                    w[2 * c][i] = (ma < pM && kc < KC)
-                                      ? __ldg(reinterpret_cast<const uint32_t *>(sfa + static_cast<size_t>(ma) * sf_ld) + kc)
+                    const int ma = m0 + lane + 32 * i;
+                    w[c][i] = (ma < pM && kc < KC)
+                                  ? __ldg(reinterpret_cast<const uint32_t *>(sfa) + static_cast<size_t>(kc) * pM + ma)
+                                  : 0u;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int nb = n0 + lane + 32 * i;
+                    w[c][4 + i] = (nb < pN && kc < KC)
+                                      ? __ldg(reinterpret_cast<const uint32_t *>(sfb) + static_cast<size_t>(kc) * pN + nb)
                                       : 0u;
-                    w[2 * c + 1][i] = (nb < pN && kc < KC)
-                                          ? __ldg(reinterpret_cast<const uint32_t *>(sfb + static_cast<size_t>(nb) * sf_ld) + kc)
-                                          : 0u;
                 }
             }
         };
-        auto write_stage = [&](int u, uint32_t (&w)[2 * kAKps][4]) -> bool {
+        auto write_stage = [&](int u, uint32_t (&w)[kAKps][12]) -> bool {
             const uint32_t gs = static_cast<uint32_t>(u);
             const int s = static_cast<int>(gs % S);
-            uint32_t got = 1;
-            if (lane == 0)
-                got = wait_phase(empty_bar(s), ((gs / S) & 1u) ^ 1u, abort_flag, status) ? 1u : 0u;
-            if (__shfl_sync(0xffffffffu, got, 0) == 0)
+            if (!__all_sync(0xffffffffu, wait_phase(empty_bar(s), ((gs / S) & 1u) ^ 1u, abort_flag, status)))
                 return false;
             tc_fence_after();
 #pragma unroll
             for (int c = 0; c < kAKps; ++c) {
                 const uint32_t col = t_lane + C::kSfStride * (s * kAKps + c);
-                tmem_st4(col, w[2 * c][0], w[2 * c][1], w[2 * c][2], w[2 * c][3]);
-                tmem_st4(col + 4, w[2 * c + 1][0], w[2 * c + 1][1], w[2 * c + 1][2], w[2 * c + 1][3]);
+                tmem_st4(col, w[c][0], w[c][1], w[c][2], w[c][3]);
+                tmem_st4(col + 4, w[c][4], w[c][5], w[c][6], w[c][7]);
+                tmem_st4(col + 8, w[c][8], w[c][9], w[c][10], w[c][11]);
             }
             tmem_wait_st();
             tc_fence_before();
             if (lane == 0)
-                mbar_arrive(sf_bar(s));
+                mbar_arrive(full_bar(s));
             return true;
         };
-        uint32_t w0[2 * kAKps][4], w1[2 * kAKps][4];
+        uint32_t w0[kAKps][12], w1[kAKps][12];
         load_words(0, w0);
         for (int u = 0; u < total; u += 2) {
             load_words(u + 1, w1);
@@ -332,30 +350,29 @@ __global__ void __launch_bounds__(AccCfg<KIND>::kThreads, 1)
     } else if (warp >= C::kEpiWarp0) {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;
-        const uint32_t stage_u32 = sbase + C::kOutOff + q * 32 * C::kOutRow;
+        const int e = warp - C::kEpiWarp0;
+        const int col0 = (e >> 2) * C::kEpiCols;                 // this warp's columns of the tile
+        const uint32_t stage_u32 = sbase + C::kOutOff + e * 32 * C::kOutRow;
         uint32_t tcount = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++tcount) {
             int m0, n0;
             tile_mn(t, m0, n0);
-            const uint32_t buf = tcount & 1u;
-            uint32_t got = 1;
-            if (lane == 0)
-                got = wait_phase(accf_bar(buf), (tcount >> 1) & 1u, abort_flag, status) ? 1u : 0u;
-            if (__shfl_sync(0xffffffffu, got, 0) == 0) {
+            const uint32_t buf = tcount % kAB;
+            if (!__all_sync(0xffffffffu, wait_phase(accf_bar(buf), (tcount / kAB) & 1u, abort_flag, status))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
+            const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + col0;
             const int rows_left = pM - (m0 + q * 32);
-            uint16_t *const d_warp = d + static_cast<size_t>(m0 + q * 32) * pN + n0;
+            uint16_t *const d_warp = d + static_cast<size_t>(m0 + q * 32) * pN + n0 + col0;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < C::kEpiCols / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld32(t_acc + c * 32, v);
                 tmem_wait_ld32(v);
-                if (c == BN / 32 - 1) {
+                if (c == C::kEpiCols / 32 - 1) {
                     // the accumulator is free for the tile after next
                     tc_fence_before();
                     if (lane == 0)
@@ -371,7 +388,7 @@ __global__ void __launch_bounds__(AccCfg<KIND>::kThreads, 1)
                                  pack_bf16x2(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5])),
                                  pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
                 __syncwarp();
-                const int cols_left = pN - (n0 + c * 32);
+                const int cols_left = pN - (n0 + col0 + c * 32);
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
                     const int rr = h * 8 + (lane >> 2);
@@ -432,7 +449,7 @@ dg_status_t launch_acc(const void *a, const uint8_t *sfa, const void *b, const u
     if (st != DG_OK)
         return st;
     const int tiles = ceil_div(M, kABM) * ceil_div(N, C::kBN);
-    AccProblem prob{M, N, K, K / 32};
+    AccProblem prob{M, N, K};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(std::min(tiles, info.sm_count));
     cfg.blockDim = dim3(C::kThreads);

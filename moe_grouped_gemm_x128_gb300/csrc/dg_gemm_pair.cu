@@ -300,12 +300,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 for (int j = 0; j < nst; ++j, ++gs) {
                     const int s = static_cast<int>(gs % kPStages);
                     const uint32_t ph = (gs / kPStages) & 1u;
-                    // the slot first, then the data: once the epilogue has
-                    // released this slot's previous use, every earlier stage
-                    // has been consumed, so the full barrier cannot be two
-                    // phases behind
-                    if (!wait_phase(tempty_bar(me), (gs & 1u) ^ 1u, abort_flag, status) ||
-                        !wait_phase(full_bar(s), ph, abort_flag, status)) {
+                    // the data first (its copies have normally landed long
+                    // before), then the slot.  This thread takes one K block
+                    // of every stage, so it has seen every earlier phase of
+                    // the stage's full barrier: the barrier is never two
+                    // phases behind when it is tested.
+                    if (!wait_phase(full_bar(s), ph, abort_flag, status) ||
+                        !wait_phase(tempty_bar(me), (gs & 1u) ^ 1u, abort_flag, status)) {
                         ok = false;
                         break;
                     }

@@ -167,8 +167,13 @@ __global__ void __launch_bounds__(256) quant_mx_1x32_kernel(const float *__restr
         const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);      // 2^-e, a normal float
         const uint32_t packed = e4m3x4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
         __stcs(reinterpret_cast<uint32_t *>(q + off), packed);
-        if ((lane & 7) == 0)
-            sx[static_cast<size_t>(r) * (K / 32) + g * 4 + (lane >> 3)] = static_cast<uint8_t>(e + 127);
+        // the group's four scale codes as one word (byte j = block j), stored
+        // chunk-major: word [g][r]
+        const uint32_t code = static_cast<uint32_t>(e + 127);
+        const uint32_t word = __shfl_sync(0xffffffffu, code, 0) | (__shfl_sync(0xffffffffu, code, 8) << 8) |
+                              (__shfl_sync(0xffffffffu, code, 16) << 16) | (__shfl_sync(0xffffffffu, code, 24) << 24);
+        if (lane == 0)
+            reinterpret_cast<uint32_t *>(sx)[static_cast<size_t>(g) * R + r] = word;
     }
 }
 

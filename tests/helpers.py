@@ -55,3 +55,16 @@ def tolerance_check(gpu: np.ndarray, ref: np.ndarray, what: str = ""):
 
 def bf16_bits_to_f32(d: np.ndarray) -> np.ndarray:
     return (d.astype(np.uint32) << 16).view(np.float32)
+
+
+def mx_scales_chunk_major(s: np.ndarray) -> np.ndarray:
+    """Row-major MX scale codes [R, K/32] in the library's chunk-major layout
+    [K/128, R, 4] (a permutation: element [g, r, j] = s[r, 4 g + j])."""
+    R, nb = s.shape
+    return np.ascontiguousarray(s.reshape(R, nb // 4, 4).transpose(1, 0, 2))
+
+
+def mx_scales_row_major(s: np.ndarray) -> np.ndarray:
+    """The inverse of mx_scales_chunk_major: [K/128, R, 4] -> [R, K/32]."""
+    G, R, _ = s.shape
+    return np.ascontiguousarray(s.transpose(1, 0, 2).reshape(R, G * 4))

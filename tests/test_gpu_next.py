@@ -10,7 +10,7 @@ import torch
 import moe_grouped_gemm_x128_gb300 as dg
 import oracle
 import workloads as wl
-from helpers import bf16_bits_to_f32, int_codes, tolerance_check
+from helpers import bf16_bits_to_f32, int_codes, mx_scales_chunk_major, mx_scales_row_major, tolerance_check
 
 pytestmark = pytest.mark.gpu
 
@@ -82,7 +82,7 @@ def test_mx_quantiser_bit_exact(R, K):
         x[R // 2, 3 * MX:4 * MX] = np.float32(448.0)  # amax exactly a power-of-two boundary case
     q, sx = dg.dg_quant_mx_1x32(dev(x))
     q_ref, sx_ref = oracle.quant_mx_1x32(x)
-    np.testing.assert_array_equal(sx.cpu().numpy(), sx_ref)
+    np.testing.assert_array_equal(mx_scales_row_major(sx.cpu().numpy()), sx_ref)
     np.testing.assert_array_equal(q.cpu().numpy(), q_ref)
 
 
@@ -101,20 +101,22 @@ def exact_mx(g, M, N, K):
 def test_mx_gemm_exact_bit_identical(M, N, K):
     g = np.random.default_rng(7 * M + N + K)
     a, sa, b, sb = exact_mx(g, M, N, K)
-    d = dg.dg_mx_gemm_nt(dev(a), dev(sa), dev(b), dev(sb))
+    d = dg.dg_mx_gemm_nt(dev(a), dev(mx_scales_chunk_major(sa)), dev(b), dev(mx_scales_chunk_major(sb)))
     np.testing.assert_array_equal(bits(d), oracle.gemm_mx_nt(a, sa, b, sb))
 
 
 def test_mx_gemm_each_block_scale_lands_on_its_block():
-    """One row of A and one of B carry a distinct scale in every 32-wide block
-    (so a scale applied to the wrong K block or the wrong row changes the
-    result); exact inputs, bit for bit."""
+    """Rows of A and of B (in both 128-row halves of a tile) carry a distinct
+    scale in every 32-wide block (so a scale applied to the wrong K block or
+    the wrong row changes the result); exact inputs, bit for bit."""
     g = np.random.default_rng(99)
     M, N, K = 256, 256, 512
     a, sa, b, sb = exact_mx(g, M, N, K)
     sa[5] = 124 + (np.arange(K // MX) % 7)
+    sa[100] = 125 + (np.arange(K // MX) % 5)
     sb[17] = 130 - (np.arange(K // MX) % 7)
-    d = dg.dg_mx_gemm_nt(dev(a), dev(sa), dev(b), dev(sb))
+    sb[200] = 124 + (np.arange(K // MX) % 6)      # the second 128-row half of a 256-wide tile
+    d = dg.dg_mx_gemm_nt(dev(a), dev(mx_scales_chunk_major(sa)), dev(b), dev(mx_scales_chunk_major(sb)))
     np.testing.assert_array_equal(bits(d), oracle.gemm_mx_nt(a, sa, b, sb))
 
 
@@ -129,7 +131,7 @@ def test_mx_quantise_then_gemm_tolerance(M, N, K):
     qa_r, sa_r = oracle.quant_mx_1x32(x)
     qb_r, sb_r = oracle.quant_mx_1x32(w)
     np.testing.assert_array_equal(qa.cpu().numpy(), qa_r)
-    np.testing.assert_array_equal(sb.cpu().numpy(), sb_r)
+    np.testing.assert_array_equal(mx_scales_row_major(sb.cpu().numpy()), sb_r)
     rows = wl.sample_rows(M, 64, 12, must=[0, M - 1, 127, 128])
     ref = oracle.gemm_mx_nt(qa_r, sa_r, qb_r, sb_r, rows=rows)
     tolerance_check(bf16_bits_to_f32(bits(d)[rows]), bf16_bits_to_f32(ref[rows]), "mx")
