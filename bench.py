@@ -701,8 +701,27 @@ def e2e(torch, dg, c: Case, args, world: int, dev) -> dict:
     ms = max_over_ranks(e0.elapsed_time(e1), device=dev)
     h2d = c.x_host.nbytes + (0 if c.meta is None else c.meta.numel() * 4)
     d2h = c.ds[0].numel() * 2
+
+    def copy_ms(dst, src, stream) -> float:
+        best = float("inf")
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            with torch.cuda.stream(stream):
+                dst.copy_(src, non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b))
+        return best
+
+    # the host link alone: one copy of the step's input, one of its output
+    h2d_ms = copy_ms(xs[0], x_pin, s_in)
+    d2h_ms = copy_ms(d_pins[0], ds[0], s_out)
+    bound = max(h2d_ms, d2h_ms)
     return {"value": job_throughput(world, c.flops, n, ms) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n,
+            "link": {"h2d_gbs": c.x_host.nbytes / (h2d_ms * 1e-3) / 1e9, "d2h_gbs": d2h / (d2h_ms * 1e-3) / 1e9,
+                     "copy_bound_ms_per_step": bound, "frac_of_copy_bound": bound / (ms / n)},
             "how": "pinned host fp32 activations in, bf16 D out, every step, three streams"}
 
 
