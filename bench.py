@@ -14,6 +14,7 @@ host cores instead (a bounded row sample of the same workload).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -203,7 +204,6 @@ def gemm_source_hash() -> str:
     """First 16 hex digits of the SHA-256 of the GEMM kernel's sources with
     comments and blank lines removed (what the compiler sees changes the hash;
     an edited comment does not)."""
-    import hashlib
     import re
     h = hashlib.sha256()
     for f in GEMM_SOURCES:
@@ -376,6 +376,12 @@ class Case:
             x, wt, masked_m = wl.masked_inputs(w)
             self.meta = t(masked_m)
         self.x_host = x
+        # fingerprints of the generated inputs (the fp32 activations and
+        # weights, and the MoE metadata), for the record
+        self.input_sha256 = {"x": hashlib.sha256(np.ascontiguousarray(x).tobytes()).hexdigest()[:16],
+                             "w": hashlib.sha256(np.ascontiguousarray(wt).tobytes()).hexdigest()[:16]}
+        if self.meta is not None:
+            self.input_sha256["meta"] = hashlib.sha256(self.meta.cpu().numpy().tobytes()).hexdigest()[:16]
         wdev = t(wt)
         self.qb, self.sfb = dg.dg_quant_weight_128x128(wdev)
         del wdev
@@ -480,7 +486,8 @@ def extra_config(torch, dg, name: str, dev, hbm: float, fp8_peak: float) -> dict
     out = {"workload": describe(w), "kernel": gemm_kernel_name(plan), "kernel_us": gemm_ms * 1e3,
            "tflops": c.flops / (gemm_ms * 1e-3) / 1e12, "useful_flop": c.flops, "algorithmic_bytes": c.bytes, **r,
            "traffic": measured_traffic(f"fp8_gemm_{name}.md"), "plan": plan,
-           "l2": c.l2_note(), "timing": f"CUDA graph of {launches} launches, replayed"}
+           "l2": c.l2_note(), "inputs_sha256": c.input_sha256,
+           "timing": f"CUDA graph of {launches} launches, replayed"}
     if w.layout == "masked":
         out["masked_m_sum"] = c.useful
     if c.has_quant:
@@ -605,7 +612,7 @@ def run_gpu(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": total_ms / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic (seeded, random init)",
-        "config": {"workload": describe(w), "l2": c.l2_note(),
+        "config": {"workload": describe(w), "l2": c.l2_note(), "inputs_sha256": c.input_sha256,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roof,
         "gpu_launches": (2 if c.has_quant else 1) * steps,
