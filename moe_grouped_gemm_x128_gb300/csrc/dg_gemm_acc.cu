@@ -38,6 +38,8 @@
 //               memory; the accumulator is released as soon as its TMEM loads
 //               are done.
 // Every wait is bounded (dg_wait.cuh).
+#include <stdlib.h>
+
 #include <algorithm>
 
 #include "dg_common.h"
@@ -413,6 +415,329 @@ __global__ void __launch_bounds__(AccCfg<KIND>::kThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// BF16 on a CTA pair: 256 x 256 tiles computed by a cluster of two CTAs that
+// share one tcgen05.mma of M = 256 (cta_group::2).  Each CTA holds its own 128
+// rows of A and half of the tile's 256 B rows, so a K chunk brings 32 KB per
+// SM per 512 MMA cycles (63 bytes per cycle), within what one SM takes in
+// through TMA (~80), where the one-SM 128 x 256 tile needs 94.  Roles, in each
+// CTA:
+//   warp 0      TMA producer of A (this CTA's 128 rows, two chunks per box);
+//   warp 1      TMA producer of B (this CTA's 128 of the tile's 256 rows); all
+//               four copies of a stage complete on rank 0's full barrier,
+//               armed by rank 0's warp 0;
+//   warp 2      allocates the TMEM of both CTAs; on rank 0, lane 0 issues every
+//               MMA into one of two accumulators (alternating by tile) and
+//               commits to both CTAs' barriers;
+//   warps 4-11  epilogue: 2 warps per TMEM lane quarter, 128 columns each;
+//               they release the accumulator on rank 0's barrier as soon as
+//               their TMEM loads are done, then store bf16.
+// Every wait is bounded (dg_wait.cuh).
+constexpr int kQRows = 128;                // rows per CTA
+constexpr int kQBN = 256;                  // columns per pair tile
+constexpr int kQStages = 3;
+constexpr int kQEpiWarp0 = 4;
+constexpr int kQEpiWarps = 8;
+constexpr int kQEpiCols = kQBN / (kQEpiWarps / 4);
+constexpr int kQThreads = 32 * (kQEpiWarp0 + kQEpiWarps);
+constexpr int kQGroupM = 8;                // pair rows per rasterisation band
+
+struct PairAccSmem {
+    static constexpr int kBox = kQRows * 128 * kAKps;         // 32 KiB
+    static constexpr int kAOff = 0;
+    static constexpr int kBOff = kAOff + kQStages * kBox;
+    static constexpr int kOutRow = 32 * 2 + 16;               // 32 bf16 columns + 16 bytes of padding
+    static constexpr int kOutOff = kBOff + kQStages * kBox;
+    static constexpr int kBarOff = kOutOff + kQEpiWarps * 32 * kOutRow;
+    // full[S], empty[S], acc_full[2], acc_empty[2], drain
+    static constexpr int kMiscOff = kBarOff + 8 * (2 * kQStages + 5);
+    static constexpr int kAlloc = kMiscOff + 16 + 1024;
+    static_assert(kAlloc <= 232448, "shared memory per CTA");
+};
+
+__global__ void __launch_bounds__(kQThreads, 1)
+    acc_pair_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                         uint16_t *__restrict__ d, AccProblem p, unsigned int *status)
+{
+    using L = PairAccSmem;
+    constexpr int S = kQStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + L::kBarOff;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::kMiscOff + 4);
+
+    const int pM = p.M, pN = p.N, pK = p.K;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair_id = blockIdx.x >> 1;
+    const int num_pairs = gridDim.x >> 1;
+    const int KC = pK / 64;                        // 128-byte chunks of 64 bf16 values
+    const int nst = (KC + kAKps - 1) / kAKps;      // stages per tile
+    const int m_blocks = (pM + 2 * kQRows - 1) / (2 * kQRows);
+    const int n_blocks = (pN + kQBN - 1) / kQBN;
+    const int num_tiles = m_blocks * n_blocks;
+    auto tile_mn = [m_blocks, n_blocks](int t, int &m0, int &n0) {
+        const int band_tiles = kQGroupM * n_blocks;
+        const int band = t / band_tiles;
+        const int first = band * kQGroupM;
+        const int band_m = min(m_blocks - first, kQGroupM);
+        const int local = t - band * band_tiles;
+        m0 = (first + local % band_m) * 2 * kQRows;
+        n0 = (local / band_m) * kQBN;
+    };
+
+    // ------------------------------------------------------------------ setup
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);          // rank 0's producer arms it; all four copies complete it
+            mbar_init(empty_bar(s), 1);         // the issuer's commit, multicast to both CTAs
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 2 * kQEpiWarps);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&tmap_a);
+        tma_prefetch_desc(&tmap_b);
+    }
+    if (warp == 2) {
+        tmem_alloc_pair(smem_u32(tmem_slot), 512);
+        tmem_relinquish_pair();
+    }
+    griddep_wait();
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    if (threadIdx.x == 0)
+        griddep_launch_dependents();
+    const uint32_t tmem_base = *tmem_slot;
+    // rank 0's copies of the shared barriers, as shared::cluster addresses
+    const uint32_t full0 = mapa_shared(full_bar(0), 0);
+    const uint32_t acce0 = mapa_shared(acce_bar(0), 0);
+
+    if (warp < 2) {
+        // ------------------------------------------------------- TMA producers
+        if (lane == 0) {
+            const bool is_a = warp == 0;
+            const CUtensorMap *map = is_a ? &tmap_a : &tmap_b;
+            const uint32_t dst0 = sbase + (is_a ? L::kAOff : L::kBOff);
+            uint32_t gs = 0;
+            bool ok = true;
+            for (int t = pair_id; ok && t < num_tiles; t += num_pairs) {
+                int m0, n0;
+                tile_mn(t, m0, n0);
+                const int row = (is_a ? m0 : n0) + static_cast<int>(rank) * kQRows;
+                for (int j = 0; j < nst; ++j, ++gs) {
+                    const int s = static_cast<int>(gs % S);
+                    if (!wait_phase(empty_bar(s), ((gs / S) & 1u) ^ 1u, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (is_a && rank == 0)
+                        mbar_arrive_expect_tx(full_bar(s), 4u * L::kBox);
+                    tma_load_3d_pair(dst0 + s * L::kBox, map, full0 + 8u * s, 0, row, j * kAKps);
+                }
+            }
+            if (!ok) {
+                // copies in flight complete on rank 0's full barriers, which
+                // this thread may not observe: give them time to land
+                const long long t0 = clock64();
+                while (clock64() - t0 < 20000000ll) {
+                }
+            }
+        }
+    } else if (warp == 2) {
+        // ---------------------------------------------------------- MMA issuer
+        if (rank == 0 && lane == 0) {
+            const uint64_t desc_a0 = smem_desc_sw128(sbase + L::kAOff);
+            const uint64_t desc_b0 = smem_desc_sw128(sbase + L::kBOff);
+            constexpr uint32_t kIdesc = idesc_bf16_f32(2 * kQRows, kQBN);
+            uint32_t gs = 0;
+            uint32_t tcount = 0;
+            bool ok = true;
+            for (int t = pair_id; ok && t < num_tiles; t += num_pairs, ++tcount) {
+                const uint32_t buf = tcount & 1u;
+                // the epilogues of both CTAs have released this accumulator
+                if (!wait_phase(acce_bar(buf), ((tcount >> 1) & 1u) ^ 1u, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * kQBN;
+                for (int j = 0; j < nst; ++j, ++gs) {
+                    const int s = static_cast<int>(gs % S);
+                    if (!wait_phase(full_bar(s), (gs / S) & 1u, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < kAKps; ++c) {
+                        const uint32_t off = static_cast<uint32_t>(s * L::kBox + c * kQRows * 128) >> 4;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t acc = (j > 0 || c > 0 || k > 0) ? 1u : 0u;
+                            mma_f16_pair(d_tmem, desc_a0 + off + 2 * k, desc_b0 + off + 2 * k, kIdesc, acc);
+                        }
+                    }
+                    mma_commit_pair_mc(empty_bar(s), 3);
+                }
+                if (!ok)
+                    break;
+                mma_commit_pair_mc(accf_bar(buf), 3);
+            }
+            // every MMA this thread issued has completed once this barrier flips
+            mma_commit_pair_mc(drain_bar, 1);
+            drain_wait(drain_bar, 0);
+        }
+    } else if (warp >= kQEpiWarp0) {
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        const int e = warp - kQEpiWarp0;
+        const int col0 = (e >> 2) * kQEpiCols;
+        const uint32_t stage_u32 = sbase + L::kOutOff + e * 32 * L::kOutRow;
+        uint32_t tcount = 0;
+        bool ok = true;
+        for (int t = pair_id; ok && t < num_tiles; t += num_pairs, ++tcount) {
+            int m0, n0;
+            tile_mn(t, m0, n0);
+            const uint32_t buf = tcount & 1u;
+            if (!__all_sync(0xffffffffu, wait_phase(accf_bar(buf), (tcount >> 1) & 1u, abort_flag, status))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kQBN + col0;
+            const int row0 = m0 + static_cast<int>(rank) * kQRows + q * 32;   // this warp's first row
+            const int rows_left = pM - row0;
+            uint16_t *const d_warp = d + static_cast<size_t>(row0) * pN + n0 + col0;
+#pragma unroll 1
+            for (int c = 0; c < kQEpiCols / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(t_acc + c * 32, v);
+                tmem_wait_ld32(v);
+                if (c == kQEpiCols / 32 - 1) {
+                    // the accumulator is free for the tile after next
+                    tc_fence_before();
+                    if (lane == 0)
+                        mbar_arrive_cluster(acce0 + 8u * buf);
+                }
+                // this thread's row: 32 bf16 values = 64 bytes, staged so that
+                // the warp stores 8 rows x 64 bytes per instruction
+                const uint32_t my_row = stage_u32 + lane * L::kOutRow;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    st_shared_v4(my_row + 16 * k, pack_bf16x2(__uint_as_float(v[8 * k]), __uint_as_float(v[8 * k + 1])),
+                                 pack_bf16x2(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3])),
+                                 pack_bf16x2(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5])),
+                                 pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
+                __syncwarp();
+                const int cols_left = pN - (n0 + col0 + c * 32);
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const int rr = h * 8 + (lane >> 2);
+                    const int cc = lane & 3;
+                    if (rr < rows_left && cc * 8 < cols_left) {
+                        const uint4 w = ld_shared_v4(stage_u32 + rr * L::kOutRow + 16 * cc);
+                        st_global_v4(d_warp + static_cast<size_t>(rr) * pN + c * 32 + cc * 8, w.x, w.y, w.z, w.w);
+                    }
+                }
+                __syncwarp();
+            }
+        }
+    }
+
+    // ------------------------------------------------------------- teardown
+    // neither CTA leaves while the other may still signal its barriers or
+    // read its tensor memory
+    tc_fence_before();
+    __syncwarp();
+    __syncthreads();
+    cluster_sync();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, 512);
+    }
+}
+
+// Pair tiles of a BF16 problem, and whether the pair kernel takes it: enough
+// 256 x 256 tiles for half the SMs' worth of pairs (otherwise the one-SM
+// kernel's 128 x 256 tiles spread the work over more SMs).  DG_FORCE_ACC_PAIR
+// = 1 / 0 overrides the choice.
+bool bf16_pair_ok(int M, int N, int num_sms)
+{
+    const char *f = getenv("DG_FORCE_ACC_PAIR");
+    if (f && f[0] == '1')
+        return num_sms >= 2;
+    if (f && f[0] == '0')
+        return false;
+    const int tiles = ceil_div(M, 2 * kQRows) * ceil_div(N, kQBN);
+    return num_sms >= 2 && tiles >= num_sms / 2;
+}
+
+dg_status_t launch_bf16_pair(const void *a, const void *b, uint16_t *d, int M, int N, int K, void *stream,
+                             const DeviceInfo &info)
+{
+    using L = PairAccSmem;
+    const uint64_t KC = static_cast<uint64_t>(K) / 64;
+    CUtensorMap ta, tb;
+    dg_status_t st;
+    {
+        // bf16 [M][K] viewed as [K/64][M][128 B]; box: 2 chunks x 128 rows
+        const uint64_t dims[3] = {64, static_cast<uint64_t>(M), KC};
+        const uint64_t strides[2] = {static_cast<uint64_t>(K) * 2, 128};
+        const uint32_t box[3] = {64, kQRows, kAKps};
+        st = encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != DG_OK)
+            return st;
+    }
+    {
+        const uint64_t dims[3] = {64, static_cast<uint64_t>(N), KC};
+        const uint64_t strides[2] = {static_cast<uint64_t>(K) * 2, 128};
+        const uint32_t box[3] = {64, kQRows, kAKps};
+        st = encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != DG_OK)
+            return st;
+    }
+    st = ensure_smem_attr(reinterpret_cast<const void *>(acc_pair_bf16_kernel), L::kAlloc);
+    if (st != DG_OK)
+        return st;
+    const int tiles = ceil_div(M, 2 * kQRows) * ceil_div(N, kQBN);
+    const int pairs = std::min(info.sm_count / 2, std::max(1, tiles));
+    AccProblem prob{M, N, K};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(kQThreads);
+    cfg.dynamicSmemBytes = L::kAlloc;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, acc_pair_bf16_kernel, ta, tb, d, prob, info.status_word) != cudaSuccess)
+        return DG_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+}
+
 template <int KIND>
 dg_status_t launch_acc(const void *a, const uint8_t *sfa, const void *b, const uint8_t *sfb, uint16_t *d, int M, int N,
                        int K, void *stream)
@@ -477,6 +802,12 @@ extern "C" dg_status_t dg_bf16_gemm_nt(const uint16_t *a, const uint16_t *b, uin
         return DG_ERR_UNSUPPORTED_SHAPE;
     if (!dg::aligned16(a) || !dg::aligned16(b) || !dg::aligned16(d))
         return DG_ERR_MISALIGNED;
+    dg::DeviceInfo info;
+    const dg_status_t st = dg::current_device(&info);
+    if (st != DG_OK)
+        return st;
+    if (dg::bf16_pair_ok(M, N, info.sm_count))
+        return dg::launch_bf16_pair(a, b, d, M, N, K, stream, info);
     return dg::launch_acc<dg::kAccKind_BF16>(a, nullptr, b, nullptr, d, M, N, K, stream);
 }
 

@@ -49,8 +49,15 @@ def to_bf16_tensor(b: np.ndarray) -> torch.Tensor:
 BF16_SHAPES = [(128, 256, 64), (1, 8, 64), (300, 520, 640), (257, 200, 1152), (1000, 1288, 384), (129, 264, 4096)]
 
 
+@pytest.fixture(params=["0", "1"], ids=["one_sm", "pair"])
+def acc_pair(request, monkeypatch):
+    """Both BF16 kernels: 128 x 256 tiles on one SM, 256 x 256 on a CTA pair."""
+    monkeypatch.setenv("DG_FORCE_ACC_PAIR", request.param)
+    return request.param
+
+
 @pytest.mark.parametrize("M,N,K", BF16_SHAPES)
-def test_bf16_integer_values_bit_identical(M, N, K):
+def test_bf16_integer_values_bit_identical(M, N, K, acc_pair):
     # integers in [-4, 4]: every product and every sum (|.| <= 16 K) is exact
     # in fp32, so the tensor core's order of summation cannot change a bit
     g = np.random.default_rng(M + N + K)
@@ -61,7 +68,7 @@ def test_bf16_integer_values_bit_identical(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(300, 520, 640), (1000, 1288, 2048)])
-def test_bf16_random_tolerance(M, N, K):
+def test_bf16_random_tolerance(M, N, K, acc_pair):
     g = np.random.default_rng(3 * M + K)
     a = bf16_of(g.standard_normal((M, K)).astype(np.float32))
     b = bf16_of(g.standard_normal((N, K)).astype(np.float32))
@@ -69,6 +76,19 @@ def test_bf16_random_tolerance(M, N, K):
     rows = wl.sample_rows(M, 64, 11, must=[0, M - 1, 127, 128])
     ref = oracle.gemm_bf16_nt(a, b, rows=rows)
     tolerance_check(bf16_bits_to_f32(bits(d)[rows]), bf16_bits_to_f32(ref[rows]), "bf16")
+
+
+def test_bf16_full_size_exact_sampled():
+    """The benchmark's BF16 shape (M=4096, N=7168, K=7168) in the plan the
+    library picks (the CTA pair), integer operands: sampled rows bit for bit."""
+    M, N, K = 4096, 7168, 7168
+    g = np.random.default_rng(4242)
+    a = bf16_of(g.integers(-2, 3, (M, K)).astype(np.float32))
+    b = bf16_of(g.integers(-2, 3, (N, K)).astype(np.float32))
+    d = dg.dg_bf16_gemm_nt(to_bf16_tensor(a), to_bf16_tensor(b))
+    rows = wl.sample_rows(M, 16, 5, must=[0, 127, 128, 255, 256, M - 1])
+    ref = oracle.gemm_bf16_nt(a, b, rows=rows)
+    np.testing.assert_array_equal(bits(d)[rows], ref[rows])
 
 
 # --------------------------------------------------------------------- MX --
