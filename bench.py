@@ -504,6 +504,16 @@ def extra_config(torch, dg, name: str, dev, hbm: float, fp8_peak: float) -> dict
 NEXT_SHAPE = (4096, 7168, 7168)   # M, N, K of the BF16 and MX legs
 
 
+def acc_kernel_name(kind: str, M: int, N: int, dev) -> str:
+    """The kernel the library picks for a BF16 or MX problem: the CTA pair
+    when there are at least half the SMs' worth of 256 x 256 tiles."""
+    import torch
+    forced = os.environ.get("DG_FORCE_ACC_PAIR", "")
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    pair = forced == "1" or (forced != "0" and -(-M // 256) * -(-N // 256) >= sms // 2)
+    return f"acc_pair_kernel<{kind}>" if pair else f"acc_gemm_kernel<{kind}>"
+
+
 def next_format_legs(torch, dg, dev, bf16_peak: float, fp8_peak: float, only: str = "") -> dict:
     """The two formats beside per-group-scaled FP8: a BF16 GEMM and an MX GEMM
     (E4M3 with an E8M0 scale per 32 K values) at M=4096, N=7168, K=7168,
@@ -521,7 +531,7 @@ def next_format_legs(torch, dg, dev, bf16_peak: float, fp8_peak: float, only: st
         a16, b16 = a32.to(torch.bfloat16), b32.to(torch.bfloat16)
         ms = graph_time_ms(torch, lambda i: dg.dg_bf16_gemm_nt(a16, b16, d), 4, 10)
         r = roofline(flops, (M * K + N * K + M * N) * 2, ms * 1e-3, 1e30, bf16_peak)
-        out["bf16"] = {"workload": f"BF16 GEMM M={M} N={N} K={K}", "kernel": "acc_gemm_kernel<bf16>",
+        out["bf16"] = {"workload": f"BF16 GEMM M={M} N={N} K={K}", "kernel": acc_kernel_name("bf16", M, N, dev),
                        "kernel_us": ms * 1e3, "tflops": flops / (ms * 1e-3) / 1e12, **r,
                        "peak_note": "measured bf16 burst peak"}
         del a16, b16
@@ -530,7 +540,7 @@ def next_format_legs(torch, dg, dev, bf16_peak: float, fp8_peak: float, only: st
         qb, sb = dg.dg_quant_mx_1x32(b32)
         ms = graph_time_ms(torch, lambda i: dg.dg_mx_gemm_nt(qa, sa, qb, sb, d), 4, 10)
         r = roofline(flops, M * K + N * K + (M + N) * K // 32 + M * N * 2, ms * 1e-3, 1e30, fp8_peak)
-        out["mx"] = {"workload": f"MX (E4M3, E8M0 per 32) GEMM M={M} N={N} K={K}", "kernel": "acc_gemm_kernel<mx>",
+        out["mx"] = {"workload": f"MX (E4M3, E8M0 per 32) GEMM M={M} N={N} K={K}", "kernel": acc_kernel_name("mx", M, N, dev),
                      "kernel_us": ms * 1e3, "tflops": flops / (ms * 1e-3) / 1e12, **r,
                      "peak_note": "measured bf16 burst peak x 2 (FP8)"}
         del qa, qb

@@ -176,7 +176,11 @@ dg_status_t dg_fp8_grouped_masked_q(const uint8_t *a, const float *sfa, const ui
 /* ------------------------------------------------------------------------
  * Beyond per-group-scaled FP8: the two formats the 2kiu.com DeepGEMM tutorial
  * names beside it.  Both keep the accumulator in tensor memory across all of
- * K (no promotion on the CUDA cores), one SM per 128-row tile.
+ * K (no promotion on the CUDA cores): 256 x 256 tiles on pairs of SMs when
+ * there are at least half the SMs' worth of them, 128 x 256 tiles on one SM
+ * otherwise (the environment variable DG_FORCE_ACC_PAIR=1 or 0 overrides the
+ * choice).  The result does not depend on the choice beyond the tensor
+ * core's summation order.
  * ------------------------------------------------------------------------ */
 
 /* BF16 GEMM (2kiu.com tutorial 1 and 2.2: BF16 beside FP8 as a

@@ -49,6 +49,36 @@
 namespace dg {
 namespace {
 
+// D[tmem] (+)= A . B^T for a CTA pair (M = 256): bf16 operands (kind::f16),
+// each CTA holding its 128 rows of A and its half of B's rows at the same
+// shared-memory offsets; D has this CTA's 128 rows in each CTA's TMEM.
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Block-scaled MX MMA for a CTA pair (M = 256, N = 256): E4M3 operands with
+// one UE8M0 scale per 32 K values.  At the same columns of each CTA's tensor
+// memory: the granule of that CTA's own 128 rows of A at sfa_tmem, and the
+// granules of all 256 rows of B at sfb_tmem (rows 0-127 in its first four
+// columns, 128-255 in the next four), found by bit-exact tests: a granule of
+// only the CTA's own half of B gave wrong columns 128-255.
+__device__ __forceinline__ void mma_mx_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 constexpr int kAccKind_BF16 = 0;
 constexpr int kAccKind_MX = 1;
 
@@ -416,33 +446,42 @@ __global__ void __launch_bounds__(AccCfg<KIND>::kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// BF16 on a CTA pair: 256 x 256 tiles computed by a cluster of two CTAs that
-// share one tcgen05.mma of M = 256 (cta_group::2).  Each CTA holds its own 128
-// rows of A and half of the tile's 256 B rows, so a K chunk brings 32 KB per
-// SM per 512 MMA cycles (63 bytes per cycle), within what one SM takes in
-// through TMA (~80), where the one-SM 128 x 256 tile needs 94.  Roles, in each
-// CTA:
+// BF16 and MX on a CTA pair: 256 x 256 tiles computed by a cluster of two CTAs
+// that share one tcgen05.mma of M = 256 (cta_group::2).  Each CTA holds its
+// own 128 rows of A and half of the tile's 256 B rows, so a K chunk brings
+// 32 KB per SM per 512 MMA cycles (63 bytes per cycle), within what one SM
+// takes in through TMA (~80), where the one-SM 128 x 256 tile needs 94.
+// Roles, in each CTA:
 //   warp 0      TMA producer of A (this CTA's 128 rows, two chunks per box);
 //   warp 1      TMA producer of B (this CTA's 128 of the tile's 256 rows); all
 //               four copies of a stage complete on rank 0's full barrier,
 //               armed by rank 0's warp 0;
 //   warp 2      allocates the TMEM of both CTAs; on rank 0, lane 0 issues every
-//               MMA into one of two accumulators (alternating by tile) and
-//               commits to both CTAs' barriers;
-//   warps 4-11  epilogue: 2 warps per TMEM lane quarter, 128 columns each;
+//               MMA and commits to both CTAs' barriers.  BF16: two
+//               accumulators alternating by tile.  MX: one accumulator (the
+//               scale columns take the room of the second);
+//   warps 4-7   (MX) scale writers: per stage and 128-wide K chunk, the
+//               granule of this CTA's 128 rows of A and the two granules of
+//               the tile's 256 rows of B (the one-SM kernel's granule layout);
+//               they arrive on rank 0's full barrier of the stage;
+//   last 8      epilogue: 2 warps per TMEM lane quarter, 128 columns each;
 //               they release the accumulator on rank 0's barrier as soon as
 //               their TMEM loads are done, then store bf16.
 // Every wait is bounded (dg_wait.cuh).
 constexpr int kQRows = 128;                // rows per CTA
 constexpr int kQBN = 256;                  // columns per pair tile
 constexpr int kQStages = 3;
-constexpr int kQEpiWarp0 = 4;
 constexpr int kQEpiWarps = 8;
 constexpr int kQEpiCols = kQBN / (kQEpiWarps / 4);
-constexpr int kQThreads = 32 * (kQEpiWarp0 + kQEpiWarps);
 constexpr int kQGroupM = 8;                // pair rows per rasterisation band
 
-struct PairAccSmem {
+template <int KIND>
+struct PairAccCfg {
+    static constexpr int kSfWarps = KIND == kAccKind_MX ? 4 : 0;
+    static constexpr int kEpiWarp0 = 4 + kSfWarps;
+    static constexpr int kThreads = 32 * (kEpiWarp0 + kQEpiWarps);
+    static constexpr int kAccBufs = KIND == kAccKind_MX ? 1 : 2;
+    static constexpr int kElemsPerChunk = KIND == kAccKind_BF16 ? 64 : 128;   // K values per 128-byte row
     static constexpr int kBox = kQRows * 128 * kAKps;         // 32 KiB
     static constexpr int kAOff = 0;
     static constexpr int kBOff = kAOff + kQStages * kBox;
@@ -452,15 +491,24 @@ struct PairAccSmem {
     // full[S], empty[S], acc_full[2], acc_empty[2], drain
     static constexpr int kMiscOff = kBarOff + 8 * (2 * kQStages + 5);
     static constexpr int kAlloc = kMiscOff + 16 + 1024;
+    // TMEM: the accumulators, then (MX) per stage and chunk one granule for
+    // A's scales and one for B's, each on its own 4-column boundary
+    static constexpr uint32_t kSfCol0 = kAccBufs * kQBN;
+    static constexpr uint32_t kSfStride = 12;                 // columns per chunk: A at +0, B rows 0-127 at +4, 128-255 at +8
     static_assert(kAlloc <= 232448, "shared memory per CTA");
+    static_assert(kSfCol0 % 4 == 0 && kSfStride % 4 == 0, "scale columns on 4-column boundaries");
+    static_assert(kAccBufs * kQBN + (KIND == kAccKind_MX ? kSfStride * kAKps * kQStages : 0) <= 512, "TMEM columns");
 };
 
-__global__ void __launch_bounds__(kQThreads, 1)
-    acc_pair_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                         uint16_t *__restrict__ d, AccProblem p, unsigned int *status)
+template <int KIND>
+__global__ void __launch_bounds__(PairAccCfg<KIND>::kThreads, 1)
+    acc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                    const uint8_t *__restrict__ sfa, const uint8_t *__restrict__ sfb, uint16_t *__restrict__ d,
+                    AccProblem p, unsigned int *status)
 {
-    using L = PairAccSmem;
+    using L = PairAccCfg<KIND>;
     constexpr int S = kQStages;
+    constexpr uint32_t kAB = L::kAccBufs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -479,7 +527,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const uint32_t rank = cluster_ctarank();
     const int pair_id = blockIdx.x >> 1;
     const int num_pairs = gridDim.x >> 1;
-    const int KC = pK / 64;                        // 128-byte chunks of 64 bf16 values
+    const int KC = pK / L::kElemsPerChunk;         // 128-byte K chunks
     const int nst = (KC + kAKps - 1) / kAKps;      // stages per tile
     const int m_blocks = (pM + 2 * kQRows - 1) / (2 * kQRows);
     const int n_blocks = (pN + kQBN - 1) / kQBN;
@@ -497,7 +545,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
     // ------------------------------------------------------------------ setup
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full_bar(s), 1);          // rank 0's producer arms it; all four copies complete it
+            // rank 0's producer arms it (and, for MX, the scale writers of
+            // both CTAs arrive); all four copies complete it
+            mbar_init(full_bar(s), 1 + 2 * L::kSfWarps);
             mbar_init(empty_bar(s), 1);         // the issuer's commit, multicast to both CTAs
         }
         for (int b = 0; b < 2; ++b) {
@@ -563,14 +613,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if (rank == 0 && lane == 0) {
             const uint64_t desc_a0 = smem_desc_sw128(sbase + L::kAOff);
             const uint64_t desc_b0 = smem_desc_sw128(sbase + L::kBOff);
-            constexpr uint32_t kIdesc = idesc_bf16_f32(2 * kQRows, kQBN);
             uint32_t gs = 0;
             uint32_t tcount = 0;
             bool ok = true;
             for (int t = pair_id; ok && t < num_tiles; t += num_pairs, ++tcount) {
-                const uint32_t buf = tcount & 1u;
+                const uint32_t buf = tcount % kAB;
                 // the epilogues of both CTAs have released this accumulator
-                if (!wait_phase(acce_bar(buf), ((tcount >> 1) & 1u) ^ 1u, abort_flag, status)) {
+                if (!wait_phase(acce_bar(buf), ((tcount / kAB) & 1u) ^ 1u, abort_flag, status)) {
                     ok = false;
                     break;
                 }
@@ -589,7 +638,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             const uint32_t acc = (j > 0 || c > 0 || k > 0) ? 1u : 0u;
-                            mma_f16_pair(d_tmem, desc_a0 + off + 2 * k, desc_b0 + off + 2 * k, kIdesc, acc);
+                            if constexpr (KIND == kAccKind_BF16) {
+                                mma_f16_pair(d_tmem, desc_a0 + off + 2 * k, desc_b0 + off + 2 * k,
+                                             idesc_bf16_f32(2 * kQRows, kQBN), acc);
+                            } else {
+                                const uint32_t sf_col = tmem_base + L::kSfCol0 + L::kSfStride * (s * kAKps + c);
+                                mma_mx_pair(d_tmem, desc_a0 + off + 2 * k, desc_b0 + off + 2 * k,
+                                            idesc_mx_e4m3(2 * kQRows, kQBN, k), sf_col, sf_col + 4, acc);
+                            }
                         }
                     }
                     mma_commit_pair_mc(empty_bar(s), 3);
@@ -602,10 +658,79 @@ __global__ void __launch_bounds__(kQThreads, 1)
             mma_commit_pair_mc(drain_bar, 1);
             drain_wait(drain_bar, 0);
         }
-    } else if (warp >= kQEpiWarp0) {
+    } else if (KIND == kAccKind_MX && warp >= 4 && warp < L::kEpiWarp0) {
+        // ------------------------------------------------------- scale writers
+        // Granule layout as in the one-SM kernel (lane l holds rows l, l + 32,
+        // l + 64, l + 96 of a 128-row block in columns 0-3, byte j = K step j,
+        // the same copy in every 32-lane quarter), for this CTA's 128 rows of
+        // A and for both 128-row halves of the tile's B.  The words of the
+        // next stage are loaded while the current one is written, into the
+        // other of two fixed register sets.
+        const int q = warp & 3;
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + L::kSfCol0;
+        const int total = ((num_tiles - pair_id + num_pairs - 1) / num_pairs) * nst;
+        auto load_words = [&](int u, uint32_t (&w)[kAKps][12]) {
+            if (u >= total)
+                return;
+            int m0, n0;
+            tile_mn(pair_id + (u / nst) * num_pairs, m0, n0);
+            const int j = u % nst;
+            const int ma0 = m0 + static_cast<int>(rank) * kQRows + lane;
+            const int nb0 = n0 + lane;
+#pragma unroll
+            for (int c = 0; c < kAKps; ++c) {
+                const int kc = j * kAKps + c;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int ma = ma0 + 32 * i;
+                    w[c][i] = (ma < pM && kc < KC)
+                                  ? __ldg(reinterpret_cast<const uint32_t *>(sfa) + static_cast<size_t>(kc) * pM + ma)
+                                  : 0u;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int nb = nb0 + 32 * i;
+                    w[c][4 + i] = (nb < pN && kc < KC)
+                                      ? __ldg(reinterpret_cast<const uint32_t *>(sfb) + static_cast<size_t>(kc) * pN + nb)
+                                      : 0u;
+                }
+            }
+        };
+        auto write_stage = [&](int u, uint32_t (&w)[kAKps][12]) -> bool {
+            const uint32_t gs = static_cast<uint32_t>(u);
+            const int s = static_cast<int>(gs % S);
+            if (!__all_sync(0xffffffffu, wait_phase(empty_bar(s), ((gs / S) & 1u) ^ 1u, abort_flag, status)))
+                return false;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < kAKps; ++c) {
+                const uint32_t col = t_lane + L::kSfStride * (s * kAKps + c);
+                tmem_st4(col, w[c][0], w[c][1], w[c][2], w[c][3]);
+                tmem_st4(col + 4, w[c][4], w[c][5], w[c][6], w[c][7]);
+                tmem_st4(col + 8, w[c][8], w[c][9], w[c][10], w[c][11]);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            if (lane == 0)
+                mbar_arrive_cluster(full0 + 8u * s);
+            return true;
+        };
+        uint32_t w0[kAKps][12], w1[kAKps][12];
+        load_words(0, w0);
+        for (int u = 0; u < total; u += 2) {
+            load_words(u + 1, w1);
+            if (!write_stage(u, w0))
+                break;
+            if (u + 1 >= total)
+                break;
+            load_words(u + 2, w0);
+            if (!write_stage(u + 1, w1))
+                break;
+        }
+    } else if (warp >= L::kEpiWarp0) {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;
-        const int e = warp - kQEpiWarp0;
+        const int e = warp - L::kEpiWarp0;
         const int col0 = (e >> 2) * kQEpiCols;
         const uint32_t stage_u32 = sbase + L::kOutOff + e * 32 * L::kOutRow;
         uint32_t tcount = 0;
@@ -613,8 +738,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
         for (int t = pair_id; ok && t < num_tiles; t += num_pairs, ++tcount) {
             int m0, n0;
             tile_mn(t, m0, n0);
-            const uint32_t buf = tcount & 1u;
-            if (!__all_sync(0xffffffffu, wait_phase(accf_bar(buf), (tcount >> 1) & 1u, abort_flag, status))) {
+            const uint32_t buf = tcount % kAB;
+            if (!__all_sync(0xffffffffu, wait_phase(accf_bar(buf), (tcount / kAB) & 1u, abort_flag, status))) {
                 ok = false;
                 break;
             }
@@ -629,7 +754,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
                 tmem_ld32(t_acc + c * 32, v);
                 tmem_wait_ld32(v);
                 if (c == kQEpiCols / 32 - 1) {
-                    // the accumulator is free for the tile after next
+                    // the accumulator is free for its next tile
                     tc_fence_before();
                     if (lane == 0)
                         mbar_arrive_cluster(acce0 + 8u * buf);
@@ -672,11 +797,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
 }
 
-// Pair tiles of a BF16 problem, and whether the pair kernel takes it: enough
-// 256 x 256 tiles for half the SMs' worth of pairs (otherwise the one-SM
-// kernel's 128 x 256 tiles spread the work over more SMs).  DG_FORCE_ACC_PAIR
-// = 1 / 0 overrides the choice.
-bool bf16_pair_ok(int M, int N, int num_sms)
+// Whether the pair kernel takes a BF16 or MX problem: enough 256 x 256 tiles
+// for half the SMs' worth of pairs (otherwise the one-SM kernel's 128 x 256
+// tiles spread the work over more SMs).  DG_FORCE_ACC_PAIR = 1 / 0 overrides.
+bool acc_pair_ok(int M, int N, int num_sms)
 {
     const char *f = getenv("DG_FORCE_ACC_PAIR");
     if (f && f[0] == '1')
@@ -687,33 +811,36 @@ bool bf16_pair_ok(int M, int N, int num_sms)
     return num_sms >= 2 && tiles >= num_sms / 2;
 }
 
-dg_status_t launch_bf16_pair(const void *a, const void *b, uint16_t *d, int M, int N, int K, void *stream,
-                             const DeviceInfo &info)
+template <int KIND>
+dg_status_t launch_acc_pair(const void *a, const uint8_t *sfa, const void *b, const uint8_t *sfb, uint16_t *d, int M,
+                            int N, int K, void *stream, const DeviceInfo &info)
 {
-    using L = PairAccSmem;
-    const uint64_t KC = static_cast<uint64_t>(K) / 64;
+    using L = PairAccCfg<KIND>;
+    // operands viewed as [K chunks][rows][128 bytes]; a box is 128 bytes x
+    // 128 rows x two chunks, 128-byte swizzled
+    const int esize = KIND == kAccKind_BF16 ? 2 : 1;
+    const CUtensorMapDataType dt = KIND == kAccKind_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const uint64_t inner = 128 / esize;
+    const uint64_t KC = static_cast<uint64_t>(K) / inner;
     CUtensorMap ta, tb;
     dg_status_t st;
     {
-        // bf16 [M][K] viewed as [K/64][M][128 B]; box: 2 chunks x 128 rows
-        const uint64_t dims[3] = {64, static_cast<uint64_t>(M), KC};
-        const uint64_t strides[2] = {static_cast<uint64_t>(K) * 2, 128};
-        const uint32_t box[3] = {64, kQRows, kAKps};
-        st = encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a, dims, strides, box,
-                               CU_TENSOR_MAP_SWIZZLE_128B);
+        const uint64_t dims[3] = {inner, static_cast<uint64_t>(M), KC};
+        const uint64_t strides[2] = {static_cast<uint64_t>(K) * esize, 128};
+        const uint32_t box[3] = {static_cast<uint32_t>(inner), kQRows, kAKps};
+        st = encode_tensor_map(&ta, dt, 3, a, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st != DG_OK)
             return st;
     }
     {
-        const uint64_t dims[3] = {64, static_cast<uint64_t>(N), KC};
-        const uint64_t strides[2] = {static_cast<uint64_t>(K) * 2, 128};
-        const uint32_t box[3] = {64, kQRows, kAKps};
-        st = encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, dims, strides, box,
-                               CU_TENSOR_MAP_SWIZZLE_128B);
+        const uint64_t dims[3] = {inner, static_cast<uint64_t>(N), KC};
+        const uint64_t strides[2] = {static_cast<uint64_t>(K) * esize, 128};
+        const uint32_t box[3] = {static_cast<uint32_t>(inner), kQRows, kAKps};
+        st = encode_tensor_map(&tb, dt, 3, b, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st != DG_OK)
             return st;
     }
-    st = ensure_smem_attr(reinterpret_cast<const void *>(acc_pair_bf16_kernel), L::kAlloc);
+    st = ensure_smem_attr(reinterpret_cast<const void *>(acc_pair_kernel<KIND>), L::kAlloc);
     if (st != DG_OK)
         return st;
     const int tiles = ceil_div(M, 2 * kQRows) * ceil_div(N, kQBN);
@@ -721,7 +848,7 @@ dg_status_t launch_bf16_pair(const void *a, const void *b, uint16_t *d, int M, i
     AccProblem prob{M, N, K};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs);
-    cfg.blockDim = dim3(kQThreads);
+    cfg.blockDim = dim3(L::kThreads);
     cfg.dynamicSmemBytes = L::kAlloc;
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[2];
@@ -733,7 +860,7 @@ dg_status_t launch_bf16_pair(const void *a, const void *b, uint16_t *d, int M, i
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, acc_pair_bf16_kernel, ta, tb, d, prob, info.status_word) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, acc_pair_kernel<KIND>, ta, tb, sfa, sfb, d, prob, info.status_word) != cudaSuccess)
         return DG_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }
@@ -806,8 +933,8 @@ extern "C" dg_status_t dg_bf16_gemm_nt(const uint16_t *a, const uint16_t *b, uin
     const dg_status_t st = dg::current_device(&info);
     if (st != DG_OK)
         return st;
-    if (dg::bf16_pair_ok(M, N, info.sm_count))
-        return dg::launch_bf16_pair(a, b, d, M, N, K, stream, info);
+    if (dg::acc_pair_ok(M, N, info.sm_count))
+        return dg::launch_acc_pair<dg::kAccKind_BF16>(a, nullptr, b, nullptr, d, M, N, K, stream, info);
     return dg::launch_acc<dg::kAccKind_BF16>(a, nullptr, b, nullptr, d, M, N, K, stream);
 }
 
@@ -820,5 +947,11 @@ extern "C" dg_status_t dg_mx_gemm_nt(const uint8_t *a, const uint8_t *sa, const 
         return DG_ERR_UNSUPPORTED_SHAPE;
     if (!dg::aligned16(a) || !dg::aligned16(sa) || !dg::aligned16(b) || !dg::aligned16(sb) || !dg::aligned16(d))
         return DG_ERR_MISALIGNED;
+    dg::DeviceInfo info;
+    const dg_status_t st = dg::current_device(&info);
+    if (st != DG_OK)
+        return st;
+    if (dg::acc_pair_ok(M, N, info.sm_count))
+        return dg::launch_acc_pair<dg::kAccKind_MX>(a, sa, b, sb, d, M, N, K, stream, info);
     return dg::launch_acc<dg::kAccKind_MX>(a, sa, b, sb, d, M, N, K, stream);
 }

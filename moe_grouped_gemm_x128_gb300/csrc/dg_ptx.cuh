@@ -279,19 +279,6 @@ __device__ __forceinline__ void mma_f8f6f4_pair(uint32_t d_tmem, uint64_t a_desc
         : "memory");
 }
 
-// D[tmem] (+)= A . B^T for a CTA pair (M = 256): bf16 operands (kind::f16),
-// each CTA holding its 128 rows of A and its half of B's rows at the same
-// shared-memory offsets; D has this CTA's 128 rows in each CTA's TMEM.
-__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // Arrive once on the mbarrier at the same shared-memory offset in each CTA of
 // `cta_mask` when every tcgen05 operation this thread issued has completed.
 __device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_mask)

@@ -118,14 +118,14 @@ def exact_mx(g, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 256), (129, 136, 128), (300, 264, 640), (1000, 520, 768), (1, 8, 384)])
-def test_mx_gemm_exact_bit_identical(M, N, K):
+def test_mx_gemm_exact_bit_identical(M, N, K, acc_pair):
     g = np.random.default_rng(7 * M + N + K)
     a, sa, b, sb = exact_mx(g, M, N, K)
     d = dg.dg_mx_gemm_nt(dev(a), dev(mx_scales_chunk_major(sa)), dev(b), dev(mx_scales_chunk_major(sb)))
     np.testing.assert_array_equal(bits(d), oracle.gemm_mx_nt(a, sa, b, sb))
 
 
-def test_mx_gemm_each_block_scale_lands_on_its_block():
+def test_mx_gemm_each_block_scale_lands_on_its_block(acc_pair):
     """Rows of A and of B (in both 128-row halves of a tile) carry a distinct
     scale in every 32-wide block (so a scale applied to the wrong K block or
     the wrong row changes the result); exact inputs, bit for bit."""
@@ -134,6 +134,7 @@ def test_mx_gemm_each_block_scale_lands_on_its_block():
     a, sa, b, sb = exact_mx(g, M, N, K)
     sa[5] = 124 + (np.arange(K // MX) % 7)
     sa[100] = 125 + (np.arange(K // MX) % 5)
+    sa[150] = 129 - (np.arange(K // MX) % 4)      # the second CTA's rows of a pair tile
     sb[17] = 130 - (np.arange(K // MX) % 7)
     sb[200] = 124 + (np.arange(K // MX) % 6)      # the second 128-row half of a 256-wide tile
     d = dg.dg_mx_gemm_nt(dev(a), dev(mx_scales_chunk_major(sa)), dev(b), dev(mx_scales_chunk_major(sb)))
@@ -141,7 +142,7 @@ def test_mx_gemm_each_block_scale_lands_on_its_block():
 
 
 @pytest.mark.parametrize("M,N,K", [(300, 520, 1024), (1000, 1288, 2048)])
-def test_mx_quantise_then_gemm_tolerance(M, N, K):
+def test_mx_quantise_then_gemm_tolerance(M, N, K, acc_pair):
     g = np.random.default_rng(M + 2 * N)
     x = wl.normal_matrix(g, (M, K), outliers=True)
     w = wl.normal_matrix(g, (N, K))
@@ -155,3 +156,20 @@ def test_mx_quantise_then_gemm_tolerance(M, N, K):
     rows = wl.sample_rows(M, 64, 12, must=[0, M - 1, 127, 128])
     ref = oracle.gemm_mx_nt(qa_r, sa_r, qb_r, sb_r, rows=rows)
     tolerance_check(bf16_bits_to_f32(bits(d)[rows]), bf16_bits_to_f32(ref[rows]), "mx")
+
+
+def test_mx_full_size_exact_sampled():
+    """The benchmark's MX shape (M=4096, N=7168, K=7168) in the plan the
+    library picks (the CTA pair), exact operands and power-of-two scales:
+    sampled rows bit for bit."""
+    M, N, K = 4096, 7168, 7168
+    g = np.random.default_rng(4343)
+    a, _, b, _ = exact_mx(g, M, N, K)
+    # scales 2^-3..2^0: block sums (|.| <= 128) scaled by at most 1 and summed
+    # over 224 blocks stay below 2^15 in multiples of 2^-6, exact in fp32
+    sa = g.integers(124, 128, (M, K // MX)).astype(np.uint8)
+    sb = g.integers(124, 128, (N, K // MX)).astype(np.uint8)
+    d = dg.dg_mx_gemm_nt(dev(a), dev(mx_scales_chunk_major(sa)), dev(b), dev(mx_scales_chunk_major(sb)))
+    rows = wl.sample_rows(M, 12, 6, must=[0, 127, 128, 255, 256, M - 1])
+    ref = oracle.gemm_mx_nt(a, sa, b, sb, rows=rows)
+    np.testing.assert_array_equal(bits(d)[rows], ref[rows])
