@@ -634,12 +634,12 @@ def run_gpu(args, w):
         line["e2e"] = e2e(torch, dg, c, args, world, dev)
 
     if rank == 0 and world == 1 and not args.no_extra:
-        configs = {}
+        others = {}
         for name in EXTRA:
             if name == w.name:
                 continue
-            configs[name] = extra_config(torch, dg, name, dev, hbm, fp8_peak)
-        line["configs"] = configs
+            others[name] = extra_config(torch, dg, name, dev, hbm, fp8_peak)
+        line["configs"] = others
         line["next_formats"] = next_format_legs(torch, dg, dev, bf16, fp8_peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, rows, el, thr = cpu_oracle_rate(w, args.cpu_seconds)

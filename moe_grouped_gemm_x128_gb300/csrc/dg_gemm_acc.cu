@@ -11,9 +11,15 @@
 //          (tcgen05.mma kind::mxf8f6f4.block_scale.scale_vec::1X): the
 //          hardware scales every 32-wide block, so there is no promotion.
 //
-// One CTA per SM, persistent, 128 x 256 tiles.  A K block of such a tile
-// brings 48 KB per 512 MMA cycles (one SM takes in at most ~80 bytes per cycle
-// through TMA), against 32 KB per 256 cycles for a 128 x 128 tile.  Roles:
+// Two kernels per format.  acc_pair_kernel (further down) computes 256 x 256
+// tiles on pairs of SMs and takes every problem with at least half the SMs'
+// worth of such tiles; acc_gemm_kernel, here, computes 128 x 256 tiles on one
+// SM and takes the smaller ones.
+//
+// acc_gemm_kernel: one CTA per SM, persistent, 128 x 256 tiles.  A K block of
+// such a tile brings 48 KB per 512 MMA cycles (one SM takes in at most ~80
+// bytes per cycle through TMA), against 32 KB per 256 cycles for a 128 x 128
+// tile.  Roles:
 //   warp 0      TMA producer of A (one box of 128 rows x two 128-byte K
 //               chunks per stage; it also arms the stage's full barrier);
 //   warp 1      TMA producer of B (256 rows x two chunks);
