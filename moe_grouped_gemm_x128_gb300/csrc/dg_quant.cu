@@ -195,29 +195,37 @@ extern "C" dg_status_t dg_quant_act_1x128(const void *x, int x_dtype, uint8_t *q
     if (st != DG_OK)
         return st;
     const int KB = K / kQBlock;
-    // four groups per warp keep four loads in flight on large problems; a small
-    // problem (less than one full wave of such tasks) takes one group per warp,
-    // spreading the division chains over more warps
-    const long long tasks4 = static_cast<long long>(ceil_div(M, kQuantWarps)) * ceil_div(KB, 4);
-    const int gpw = tasks4 >= info.sm_count * 8LL ? 4 : 1;
-    const long long tasks = static_cast<long long>(ceil_div(M, kQuantWarps)) * ceil_div(KB, gpw);
-    const int grid = static_cast<int>(tasks < info.sm_count * 8LL ? tasks : info.sm_count * 8LL);
+    // eight groups per warp keep eight 16-byte loads per lane in flight on
+    // large problems (33152 x 7168 fp32: 191 against 213 us with four); a
+    // problem with less than a full wave of such tasks takes four, and a small
+    // one (less than a wave of four-group tasks) one group per warp, spreading
+    // the division chains over more warps
+    const long long rows8 = ceil_div(M, kQuantWarps);
+    const long long wave = info.sm_count * 8LL;
+    const int gpw = rows8 * ceil_div(KB, 8) >= wave ? 8 : rows8 * ceil_div(KB, 4) >= wave ? 4 : 1;
+    const long long tasks = rows8 * ceil_div(KB, gpw);
+    const int grid = static_cast<int>(tasks < wave ? tasks : wave);
     const int ldsfa = round_up(M, 4);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto run = [&](auto kernel, const auto *xt) {
+        kernel<<<grid, kQuantWarps * 32, 0, s>>>(xt, q, sfa, M, K, ldsfa);
+    };
     if (x_dtype == DG_DTYPE_F32) {
-        if (gpw == 4)
-            quant_act_1x128_kernel<float, 4><<<grid, kQuantWarps * 32, 0, s>>>(static_cast<const float *>(x), q, sfa,
-                                                                                M, K, ldsfa);
+        const float *xf = static_cast<const float *>(x);
+        if (gpw == 8)
+            run(quant_act_1x128_kernel<float, 8>, xf);
+        else if (gpw == 4)
+            run(quant_act_1x128_kernel<float, 4>, xf);
         else
-            quant_act_1x128_kernel<float, 1><<<grid, kQuantWarps * 32, 0, s>>>(static_cast<const float *>(x), q, sfa,
-                                                                                M, K, ldsfa);
+            run(quant_act_1x128_kernel<float, 1>, xf);
     } else {
-        if (gpw == 4)
-            quant_act_1x128_kernel<uint16_t, 4><<<grid, kQuantWarps * 32, 0, s>>>(static_cast<const uint16_t *>(x), q,
-                                                                                   sfa, M, K, ldsfa);
+        const uint16_t *xh = static_cast<const uint16_t *>(x);
+        if (gpw == 8)
+            run(quant_act_1x128_kernel<uint16_t, 8>, xh);
+        else if (gpw == 4)
+            run(quant_act_1x128_kernel<uint16_t, 4>, xh);
         else
-            quant_act_1x128_kernel<uint16_t, 1><<<grid, kQuantWarps * 32, 0, s>>>(static_cast<const uint16_t *>(x), q,
-                                                                                   sfa, M, K, ldsfa);
+            run(quant_act_1x128_kernel<uint16_t, 1>, xh);
     }
     return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }
