@@ -252,9 +252,52 @@ def job_throughput(world: int, units_per_rank_step: float, steps: int, max_ms: f
 
 
 # ---------------------------------------------------------------- CPU leg --
-def _contig_sample_setup(w: wl.Workload):
+def host_inputs(w: wl.Workload):
+    """The workload's seeded host inputs: fp32 activations, fp32 weights and
+    the MoE metadata (m_indices or masked_m; None for dense)."""
+    if w.layout == "dense":
+        x, wt = wl.dense_inputs(w.M, w.N, w.K, w.seed, w.outliers)
+        return x, wt, None
+    if w.layout == "contiguous":
+        x, wt, m_indices, _ = wl.contiguous_inputs(w)
+        return x, wt, m_indices
+    x, wt, masked_m = wl.masked_inputs(w)
+    return x, wt, masked_m
+
+
+def input_fingerprints(x, wt, meta) -> dict:
+    """First 16 hex digits of the SHA-256 of each generated input, for the record."""
+    f = {"x": hashlib.sha256(np.ascontiguousarray(x).tobytes()).hexdigest()[:16],
+         "w": hashlib.sha256(np.ascontiguousarray(wt).tobytes()).hexdigest()[:16]}
+    if meta is not None:
+        f["meta"] = hashlib.sha256(np.ascontiguousarray(meta).tobytes()).hexdigest()[:16]
+    return f
+
+
+def input_sets(w: wl.Workload, x_bytes: int, min_sets: int = 1):
+    """Bytes of one step's activations, codes and output, and how many
+    independent copies make the steps' inputs exceed 2x L2."""
+    rows, _, N, K, _ = gemm_shape(w)
+    set_bytes = x_bytes + rows * K + rows * N * 2
+    return set_bytes, max(min_sets, -(-2 * L2_BYTES // set_bytes))
+
+
+def l2_note(set_bytes: int, n_sets: int) -> str:
+    if n_sets > 1:
+        return f"rotating {n_sets} input sets of {set_bytes / 1e6:.1f} MB (> 2x L2) between launches"
+    return f"inputs of {set_bytes / 1e6:.0f} MB per step (> 2x L2)"
+
+
+def run_config(w: wl.Workload, x, wt, meta, world: int) -> dict:
+    """The `config` object of the JSON line; both arms print the same one."""
+    set_bytes, n_sets = input_sets(w, x.nbytes)
+    return {"workload": describe(w), "l2": l2_note(set_bytes, n_sets), "inputs_sha256": input_fingerprints(x, wt, meta),
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+def _contig_sample_setup(w: wl.Workload, inputs=None):
     import oracle
-    x, wt, m_indices, counts = wl.contiguous_inputs(w)
+    x, wt, m_indices = inputs if inputs is not None else host_inputs(w)
     qb, sfb = oracle.quant_weight_128x128(wt)
     a_full = np.zeros((len(m_indices), w.K), np.uint8)
     sfa_full = np.zeros((w.K // 128, oracle.round_up(len(m_indices), 4)), np.float32)
@@ -279,14 +322,14 @@ def _oracle_rows(w: wl.Workload, state, rows: np.ndarray):
     oracle.grouped_contiguous(a_full, sfa_full, qb, sfb, m_indices, rows=rows)
 
 
-def _oracle_state(w: wl.Workload):
+def _oracle_state(w: wl.Workload, inputs=None):
     import oracle
     if w.layout == "dense":
-        x, wt = wl.dense_inputs(w.M, w.N, w.K, w.seed, w.outliers)
+        x, wt, _ = inputs if inputs is not None else host_inputs(w)
         qb, sfb = oracle.quant_weight_128x128(wt)
         return (x, qb, sfb), np.arange(w.M)
     if w.layout == "contiguous":
-        st = _contig_sample_setup(w)
+        st = _contig_sample_setup(w, inputs)
         return st, st[-1]
     raise SystemExit("the CPU leg covers the dense and contiguous workloads")
 
@@ -321,7 +364,10 @@ def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    state, rows_all = _oracle_state(w)
+    inputs = host_inputs(w)
+    config = run_config(w, *inputs, args.gpus)
+    state, rows_all = _oracle_state(w, inputs)
+    del inputs
     thr = oracle.num_threads()
     rows_per_step = min(len(rows_all), thr)
     order = np.random.default_rng(99).permutation(rows_all)
@@ -342,7 +388,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 block sums, fp32 promotion",
-        "data": "synthetic", "config": {"workload": describe(w)},
+        "data": "synthetic", "config": config,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
                          "sample": f"per step {rows_per_step} of {rows_total} rows x all {w.N} columns "
                                    f"(quantise + GEMM), {elapsed:.1f} s timed"},
@@ -366,28 +412,14 @@ class Case:
         self.flops = useful_flops(w)
         self.bytes = algorithmic_bytes(w)
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-        if w.layout == "dense":
-            x, wt = wl.dense_inputs(w.M, N, K, w.seed, w.outliers)
-            self.meta = None
-        elif w.layout == "contiguous":
-            x, wt, m_indices, _ = wl.contiguous_inputs(w)
-            self.meta = t(m_indices)
-        else:
-            x, wt, masked_m = wl.masked_inputs(w)
-            self.meta = t(masked_m)
+        x, wt, meta = host_inputs(w)
+        self.meta = None if meta is None else t(meta)
         self.x_host = x
-        # fingerprints of the generated inputs (the fp32 activations and
-        # weights, and the MoE metadata), for the record
-        self.input_sha256 = {"x": hashlib.sha256(np.ascontiguousarray(x).tobytes()).hexdigest()[:16],
-                             "w": hashlib.sha256(np.ascontiguousarray(wt).tobytes()).hexdigest()[:16]}
-        if self.meta is not None:
-            self.input_sha256["meta"] = hashlib.sha256(self.meta.cpu().numpy().tobytes()).hexdigest()[:16]
+        self.input_sha256 = input_fingerprints(x, wt, meta)
         wdev = t(wt)
         self.qb, self.sfb = dg.dg_quant_weight_128x128(wdev)
         del wdev
-        set_bytes = x.nbytes + rows * K + rows * N * 2
-        self.set_bytes = set_bytes
-        self.n_sets = max(min_sets, -(-2 * L2_BYTES // set_bytes))
+        self.set_bytes, self.n_sets = input_sets(w, x.nbytes, min_sets)
         self.xs, self.qas, self.sfas, self.ds = [], [], [], []
         xdev = t(x)
         for i in range(self.n_sets):
@@ -439,9 +471,7 @@ class Case:
         self.gemm(j, stream)
 
     def l2_note(self) -> str:
-        if self.n_sets > 1:
-            return f"rotating {self.n_sets} input sets of {self.set_bytes / 1e6:.1f} MB (> 2x L2) between launches"
-        return f"inputs of {self.set_bytes / 1e6:.0f} MB per step (> 2x L2)"
+        return l2_note(self.set_bytes, self.n_sets)
 
 
 def gemm_kernel_name(plan: dict) -> str:
@@ -623,7 +653,7 @@ def run_gpu(args, w):
         "warmup": args.warmup, "ms_per_step": total_ms / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic (seeded, random init)",
         "config": {"workload": describe(w), "l2": c.l2_note(), "inputs_sha256": c.input_sha256,
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "parallelism": "replicas" if world > 1 else "single GPU"},   # = run_config()
         "roofline": roof,
         "gpu_launches": (2 if c.has_quant else 1) * steps,
         "launch": "direct launches on one stream with CUDA events around each kernel",

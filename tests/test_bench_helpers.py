@@ -97,3 +97,19 @@ def test_reduced_token_count_is_a_profiling_variant_only():
     w = bench.with_tokens(wl.WORKLOADS["contig"], 4096)
     assert w.tokens == 4096 and w.name != "contig" and w.N == 4096 and w.K == 7168
     assert bench.with_tokens(wl.WORKLOADS["skinny"], 4096) is wl.WORKLOADS["skinny"]
+
+
+def test_both_arms_print_the_same_config():
+    """The reference arm's config is the GPU arm's: same workload text, L2
+    note and input fingerprints, computed from the same seeded host inputs."""
+    w = wl.WORKLOADS["skinny"]
+    x, wt, meta = bench.host_inputs(w)
+    cfg = bench.run_config(w, x, wt, meta, 1)
+    assert set(cfg) == {"workload", "l2", "inputs_sha256", "parallelism"}
+    assert cfg == bench.run_config(w, *bench.host_inputs(w), 1)          # deterministic
+    set_bytes, n_sets = bench.input_sets(w, x.nbytes)
+    assert n_sets * set_bytes >= 2 * bench.L2_BYTES and cfg["l2"] == bench.l2_note(set_bytes, n_sets)
+    assert cfg["parallelism"] == "single GPU" and bench.run_config(w, x, wt, meta, 2)["parallelism"] == "replicas"
+    # a different seed changes the fingerprints
+    x2, wt2 = wl.dense_inputs(w.M, w.N, w.K, w.seed + 1, w.outliers)
+    assert bench.input_fingerprints(x2, wt2, None) != cfg["inputs_sha256"]
