@@ -56,8 +56,8 @@ def parse(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--profile-next", default="", choices=["", "bf16", "mx"],
-                    help="run only the BF16 or MX GEMM leg a few times (profiling aid; not a bench line)")
+    ap.add_argument("--profile-next", default="", choices=["", "bf16", "mx", "requant"],
+                    help="run only the BF16, MX or re-quantised-output leg (profiling aid; not a bench line)")
     return ap.parse_args(argv)
 
 
@@ -575,8 +575,45 @@ def next_format_legs(torch, dg, dev, bf16_peak: float, fp8_peak: float, only: st
                      "peak_note": "measured bf16 burst peak x 2 (FP8)"}
         del qa, qb
     del a32, b32, d
+    if only in ("", "requant"):
+        out["requant"] = requant_leg(torch, dg, dev)
     torch.cuda.empty_cache()
     return out
+
+
+REQUANT_SHAPE = (4096, 7168, 2048)   # M, N, K of the re-quantised-output leg
+
+
+def requant_leg(torch, dg, dev) -> dict:
+    """The FP8 GEMM with its output re-quantised in the epilogue (E4M3 codes +
+    1x128 scales, the next GEMM's activation operand) against the two calls it
+    replaces (bf16 GEMM, then the quantiser on bf16 D), dense M=4096, N=7168,
+    K=2048, seeded N(0,1) inputs, CUDA graphs of repeated launches."""
+    M, N, K = REQUANT_SHAPE
+    g = torch.Generator(device=dev)
+    g.manual_seed(12)
+    qa, sa = dg.dg_quant_act_1x128(torch.randn((M, K), generator=g, device=dev))
+    qb, sb = dg.dg_quant_weight_128x128(torch.randn((N, K), generator=g, device=dev))
+    q = torch.empty((M, N), dtype=torch.uint8, device=dev)
+    so = torch.zeros((N // 128, dg.round_up(M, 4)), dtype=torch.float32, device=dev)
+    d = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    q2 = torch.empty_like(q)
+    so2 = torch.zeros_like(so)
+    fused = graph_time_ms(torch, lambda i: dg.dg_fp8_gemm_nt_q(qa, sa, qb, sb, q, so), 4, 10)
+
+    def two_calls(i):
+        dg.dg_fp8_gemm_nt(qa, sa, qb, sb, d)
+        dg.dg_quant_act_1x128(d, q2, so2)
+
+    pair = graph_time_ms(torch, two_calls, 4, 10)
+    gemm_only = graph_time_ms(torch, lambda i: dg.dg_fp8_gemm_nt(qa, sa, qb, sb, d), 4, 10)
+    flops = 2.0 * M * N * K
+    out_bytes = M * N + (N // 128) * M * 4
+    return {"workload": f"dense FP8 GEMM M={M} N={N} K={K}, output re-quantised (E4M3 + 1x128 scales)",
+            "kernel": "fp8_gemm_kernel<128, 5, 64, 1, true>", "fused_us": fused * 1e3,
+            "two_calls_us": pair * 1e3, "bf16_gemm_alone_us": gemm_only * 1e3,
+            "fused_tflops": flops / (fused * 1e-3) / 1e12, "speedup_over_two_calls": pair / fused,
+            "output_bytes": out_bytes}
 
 
 def run_gpu(args, w):
