@@ -59,7 +59,7 @@ namespace {
 constexpr int kPRowsCta = 128;             // rows per CTA (TMEM lanes)
 constexpr int kPBN = 256;                  // columns per pair tile
 constexpr int kPKps = 2;                   // K blocks per stage (one box per operand per CTA)
-constexpr int kPStages = 3;
+constexpr int kPStages = 2;
 constexpr int kPEpiWarp0 = 4;
 constexpr int kPEpiWarps = 16;             // 4 warpgroups x 64 columns
 constexpr int kPEpiCols = 64;
@@ -71,9 +71,9 @@ struct PairSmem {
     static constexpr int kBox = kPRowsCta * 128 * kPKps;       // 32 KiB: 128 rows x 2 K blocks
     static constexpr int kAOff = 0;
     static constexpr int kBOff = kAOff + kPStages * kBox;
-    // output staging: per epilogue warp 32 rows x 32 bytes (16 bf16 columns
-    // per pass, four passes), 16-byte chunks swizzled against bank conflicts
-    static constexpr int kOutWarpBytes = 32 * 32;
+    // output staging: per epilogue warp its 32 rows x 64 bf16 columns (128
+    // bytes a row), in the 128-byte swizzled order of the output's TMA store
+    static constexpr int kOutWarpBytes = 32 * 128;
     static constexpr int kOutOff = kBOff + kPStages * kBox;
     // scales: per epilogue warp and stage parity, sfa of its 32 rows for the
     // stage's two K blocks and the two sfb values of its column block
@@ -88,6 +88,31 @@ struct PairSmem {
     static constexpr int kAlloc = kBytes + 1024;              // slack to align the base to 1024
     static_assert(kNumBars * 8 <= 128, "barrier area");
 };
+
+// TMA store of a [32 rows][64 bf16] box from this CTA's shared memory (128-byte
+// swizzled) to D at (column x, row y); the bulk-group bookkeeping of the
+// issuing thread.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the shared-memory sources of this thread's bulk stores have been read
+__device__ __forceinline__ void bulk_wait_group_read0()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// this thread's bulk stores have completed
+__device__ __forceinline__ void bulk_wait_group0()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 
 struct PairProblem {
     int M;        // dense: rows; contiguous: sum_M
@@ -137,6 +162,7 @@ __device__ __forceinline__ PairTile pair_tile(int t, int rows_p, int n_blocks, i
 
 __global__ void __launch_bounds__(kPThreads, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                         const __grid_constant__ CUtensorMap tmap_d,
                          const float *__restrict__ sfa, const float *__restrict__ sfb, uint16_t *__restrict__ d,
                          const int32_t *__restrict__ meta, PairProblem p, unsigned int *status)
 {
@@ -440,30 +466,44 @@ __global__ void __launch_bounds__(kPThreads, 1)
             for (int k = 0; k < kPEpiCols / 2; ++k)
                 pk[k] = pack_bf16x2(acc[k].x, acc[k].y);
             const uint32_t rows_ok = __ballot_sync(0xffffffffu, row_ok);
-            uint16_t *const d_warp = d + static_cast<size_t>(ti.m_cta + q * 32) * pN + ti.n0 + c0;
             const int cols_left = pN - (ti.n0 + c0);
-            const int sw = (lane >> 2) & 1;
+            // The warp's 32 rows x 64 columns go into its staging rows in the
+            // 128-byte swizzled order (chunk c of row r at c ^ (r & 7): the
+            // lanes' 16-byte writes fall in distinct banks).  When all 32 rows
+            // are stored, one TMA store writes them (clipped at the M and N
+            // edges) and the warp moves on; otherwise (contiguous padding
+            // rows, a rank with no rows) the warp stores the rows it owns.
+            if (lane == 0)
+                bulk_wait_group_read0();        // the previous tile's store has read the staging rows
+            __syncwarp();
 #pragma unroll
-            for (int pass = 0; pass < kPEpiCols / 16; ++pass) {
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int k = pass * 8 + c * 4;
-                    st_shared_v4(stage_u32 + lane * 32 + 16 * (c ^ sw), pk[k], pk[k + 1], pk[k + 2], pk[k + 3]);
-                }
+            for (int c = 0; c < 8; ++c)
+                st_shared_v4(stage_u32 + lane * 128 + 16 * (c ^ (lane & 7)), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                             pk[4 * c + 3]);
+            if (rows_ok == 0xFFFFFFFFu && cols_left > 0) {
+                fence_proxy_async_smem();       // the writes above, visible to the TMA engine
                 __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmap_d, stage_u32, ti.n0 + c0, ti.m_cta + q * 32);
+                    bulk_commit_group();
+                }
+            } else {
+                __syncwarp();
+                uint16_t *const d_warp = d + static_cast<size_t>(ti.m_cta + q * 32) * pN + ti.n0 + c0;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int rr = h * 16 + (lane >> 1);
-                    const int cc = lane & 1;
-                    const int col = pass * 16 + cc * 8;
-                    if (((rows_ok >> rr) & 1u) && col < cols_left) {
-                        const uint4 v = ld_shared_v4(stage_u32 + rr * 32 + 16 * (cc ^ ((rr >> 2) & 1)));
-                        st_global_v4(d_warp + static_cast<size_t>(rr) * pN + col, v.x, v.y, v.z, v.w);
+                for (int i = 0; i < 8; ++i) {
+                    const int rr = i * 4 + (lane >> 3);
+                    const int cc = lane & 7;
+                    if (((rows_ok >> rr) & 1u) && cc * 8 < cols_left) {
+                        const uint4 v = ld_shared_v4(stage_u32 + rr * 128 + 16 * (cc ^ (rr & 7)));
+                        st_global_v4(d_warp + static_cast<size_t>(rr) * pN + cc * 8, v.x, v.y, v.z, v.w);
                     }
                 }
-                __syncwarp();
             }
         }
+        // every bulk store of this thread has completed before the CTA ends
+        if (lane == 0)
+            bulk_wait_group0();
     }
 
     // ------------------------------------------------------------- teardown
@@ -538,6 +578,18 @@ dg_status_t launch_pair(int layout, const uint8_t *a, const float *sfa, const ui
         if (st != DG_OK)
             return st;
     }
+    CUtensorMap td;
+    {
+        // D: bf16 [M][N]; box: 64 columns x 32 rows (one epilogue warp's part
+        // of a tile), 128-byte swizzled like the staging rows
+        const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(N) * 2};
+        const uint32_t box[2] = {static_cast<uint32_t>(kPEpiCols), 32};
+        st = encode_tensor_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != DG_OK)
+            return st;
+    }
     st = ensure_smem_attr(reinterpret_cast<const void *>(fp8_gemm_pair_kernel), PairSmem::kAlloc);
     if (st != DG_OK)
         return st;
@@ -558,7 +610,7 @@ dg_status_t launch_pair(int layout, const uint8_t *a, const float *sfa, const ui
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, fp8_gemm_pair_kernel, ta, tb, sfa, sfb, d, meta, prob, info.status_word) !=
+    if (cudaLaunchKernelEx(&cfg, fp8_gemm_pair_kernel, ta, tb, td, sfa, sfb, d, meta, prob, info.status_word) !=
         cudaSuccess)
         return DG_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
