@@ -192,12 +192,14 @@ constexpr int max_regs()
 template <int BN, int STAGES, int EPI_COLS, int KPS, bool QOUT>
 __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1) __maxnreg__(max_regs<BN>())
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                    const float *__restrict__ sfa, const float *__restrict__ sfb,
+                    const __grid_constant__ CUtensorMap tmap_d, const float *__restrict__ sfa, const float *__restrict__ sfb,
                     uint16_t *__restrict__ d, uint8_t *__restrict__ qout, float *__restrict__ sfo,
                     const int32_t *__restrict__ meta, Problem p, unsigned int *status)
 {
     using L = SmemLayout<BN, STAGES, EPI_COLS, KPS>;
     static_assert(!QOUT || (BN == 128 && EPI_COLS == 64), "re-quantised output needs one 128-column group per tile");
+    static_assert(EPI_COLS != 64 || (L::kOutOff % 1024 == 0 && L::kOutWarpBytes >= 4096),
+                  "64-column warps stage 4 KiB each on 1 KiB boundaries for the output's TMA store");
     constexpr int kNumEpiWarps = Roles<BN, EPI_COLS>::kNumEpiWarps;
     // TMEM slots: one per ring stage in flight between the MMAs and the
     // epilogue, each holding the KPS partial products (128 x BN fp32) of one
@@ -634,7 +636,47 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1) __maxnreg__(
             // then the warp writes 32 rows x kCols out row-major, so that one
             // instruction covers whole row segments.  Rows that must not be
             // written (edges, masked tails, padding) are skipped.
-            if constexpr (!QOUT) {
+            if constexpr (!QOUT && kCols == 64) {
+                // 64-column warps: 32 rows x 128 bytes in the 128-byte
+                // swizzled order of the output's TMA store (chunk c of row r
+                // at c ^ (r & 7), so the lanes' 16-byte writes fall in
+                // distinct banks), 4 KiB per warp on a 1 KiB boundary.  When
+                // all 32 rows are stored, one TMA store writes them (clipped
+                // at the N edge) and the warp moves on; otherwise (edges,
+                // masked tails, padding) the warp stores the rows it owns.
+                const uint32_t st0 = smem_u32(smem + L::kOutOff) + (warp - kEpiWarp0) * 4096;
+                if (lane == 0)
+                    bulk_wait_group_read0();      // the previous tile's store has read these rows
+                __syncwarp();
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(st0 + lane * 128 + 16 * (c ^ (lane & 7)), pack_bf16x2(acc[c * 4 + 0].x, acc[c * 4 + 0].y),
+                                 pack_bf16x2(acc[c * 4 + 1].x, acc[c * 4 + 1].y),
+                                 pack_bf16x2(acc[c * 4 + 2].x, acc[c * 4 + 2].y),
+                                 pack_bf16x2(acc[c * 4 + 3].x, acc[c * 4 + 3].y));
+                const uint32_t rows_ok = __ballot_sync(0xffffffffu, row_ok);
+                const size_t warp_row0 = d_row - lane;           // D row of this warp's first row
+                const int cols_left = p.N - (ti.n0 + c0);
+                if (rows_ok == 0xFFFFFFFFu && cols_left > 0) {
+                    fence_proxy_async_smem();     // the writes above, visible to the TMA engine
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmap_d, st0, ti.n0 + c0, static_cast<int>(warp_row0));
+                        bulk_commit_group();
+                    }
+                } else {
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = i * 4 + (lane >> 3);
+                        const int cc = lane & 7;
+                        if (((rows_ok >> rr) & 1u) && cc * 8 < cols_left) {
+                            const uint4 v = ld_shared_v4(st0 + rr * 128 + 16 * (cc ^ (rr & 7)));
+                            st_global_v4(d + (warp_row0 + rr) * p.N + ti.n0 + c0 + cc * 8, v.x, v.y, v.z, v.w);
+                        }
+                    }
+                }
+            } else if constexpr (!QOUT) {
                 uint8_t *const stage = smem + L::kOutOff + (warp - kEpiWarp0) * L::kOutWarpBytes;
                 const uint32_t my_row = smem_u32(stage) + lane * L::kOutRowStride;
 #pragma unroll
@@ -737,6 +779,9 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1) __maxnreg__(
                 tile_par ^= 1u;
             }
         }
+        // every bulk store of this thread has completed before the CTA ends
+        if (lane == 0)
+            bulk_wait_group0();
     }
 
     // ------------------------------------------------------------- teardown
@@ -912,6 +957,20 @@ dg_status_t launch(int layout, const uint8_t *a, const float *sfa, const uint8_t
         if (st != DG_OK)
             return st;
     }
+    // D (bf16 output): [rows][N], masked [G x max_m][N]; box: one 64-column
+    // epilogue warp's 32 rows, 128-byte swizzled like its staging rows.  The
+    // re-quantised output has no bf16 D and never reads this map.
+    CUtensorMap td{};
+    if (d) {
+        const uint64_t rows = layout == DG_LAYOUT_MASKED ? static_cast<uint64_t>(G) * M : static_cast<uint64_t>(M);
+        const uint64_t dims[2] = {static_cast<uint64_t>(N), rows};
+        const uint64_t strides[1] = {static_cast<uint64_t>(N) * 2};
+        const uint32_t box[2] = {64, 32};
+        st = encode_tensor_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != DG_OK)
+            return st;
+    }
     auto kernel = qmode         ? fp8_gemm_kernel<128, kCfg128.stages, kCfg128.epi_cols, kCfg128.kps, true>
                   : pl.bn == 192 ? fp8_gemm_kernel<192, kCfg192.stages, kCfg192.epi_cols, kCfg192.kps, false>
                   : pl.bn == 96  ? fp8_gemm_kernel<96, kCfg96.stages, kCfg96.epi_cols, kCfg96.kps, false>
@@ -933,7 +992,8 @@ dg_status_t launch(int layout, const uint8_t *a, const float *sfa, const uint8_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, sfa, sfb, d, qout, sfo, meta, prob, info.status_word) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, td, sfa, sfb, d, qout, sfo, meta, prob, info.status_word) !=
+        cudaSuccess)
         return DG_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }

@@ -89,31 +89,6 @@ struct PairSmem {
     static_assert(kNumBars * 8 <= 128, "barrier area");
 };
 
-// TMA store of a [32 rows][64 bf16] box from this CTA's shared memory (128-byte
-// swizzled) to D at (column x, row y); the bulk-group bookkeeping of the
-// issuing thread.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y)
-{
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(src), "r"(x), "r"(y)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group()
-{
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// the shared-memory sources of this thread's bulk stores have been read
-__device__ __forceinline__ void bulk_wait_group_read0()
-{
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// this thread's bulk stores have completed
-__device__ __forceinline__ void bulk_wait_group0()
-{
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 struct PairProblem {
     int M;        // dense: rows; contiguous: sum_M
     int N;

@@ -365,6 +365,31 @@ __device__ __forceinline__ void tmem_wait_ld16(uint32_t (&r)[16])
                  : "memory");
 }
 
+// TMA store of a 2-D box from this CTA's shared memory (in the tensor map's
+// swizzled order) to global memory at (x, y); the bulk-group bookkeeping of
+// the issuing thread.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the shared-memory sources of this thread's bulk stores have been read
+__device__ __forceinline__ void bulk_wait_group_read0()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// this thread's bulk stores have completed
+__device__ __forceinline__ void bulk_wait_group0()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
 // with 128-byte swizzling: rows of 128 bytes, 8-row swizzle atoms 1024 bytes
 // apart (stride byte offset), tile base 1024-byte aligned.  Fields: start
