@@ -82,9 +82,10 @@ struct SmemLayout {
     static constexpr int kBBytes = KPS * kBSub;
     static constexpr int kAOff = 0;
     static constexpr int kBOff = kAOff + STAGES * kABytes;
-    // output staging: each epilogue warp owns 32 rows x EPI_COLS bf16, rows
-    // padded by 16 bytes so that row-per-thread 16-byte writes do not collide
-    // on shared-memory banks
+    // output staging: each epilogue warp owns 32 rows x EPI_COLS bf16.  The
+    // bf16 store uses the first 32 x 2 EPI_COLS bytes in its TMA store's
+    // swizzled order; the re-quantised output pads its rows by 16 bytes so
+    // that row-per-thread 16-byte writes do not collide on shared-memory banks
     static constexpr int kOutRowStride = EPI_COLS * 2 + 16;
     static constexpr int kOutWarpBytes = 32 * kOutRowStride;
     static constexpr int kOutOff = kBOff + STAGES * kBBytes;
@@ -198,8 +199,9 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1) __maxnreg__(
 {
     using L = SmemLayout<BN, STAGES, EPI_COLS, KPS>;
     static_assert(!QOUT || (BN == 128 && EPI_COLS == 64), "re-quantised output needs one 128-column group per tile");
-    static_assert(EPI_COLS != 64 || (L::kOutOff % 1024 == 0 && L::kOutWarpBytes >= 4096),
-                  "64-column warps stage 4 KiB each on 1 KiB boundaries for the output's TMA store");
+    static_assert(QOUT || ((EPI_COLS == 32 || EPI_COLS == 64) && L::kOutOff % 1024 == 0 &&
+                           L::kOutWarpBytes >= 32 * EPI_COLS * 2),
+                  "bf16 output: each warp stages 32 rows x EPI_COLS on a swizzle-aligned boundary for its TMA store");
     constexpr int kNumEpiWarps = Roles<BN, EPI_COLS>::kNumEpiWarps;
     // TMEM slots: one per ring stage in flight between the MMAs and the
     // epilogue, each holding the KPS partial products (128 x BN fp32) of one
@@ -636,21 +638,26 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1) __maxnreg__(
             // then the warp writes 32 rows x kCols out row-major, so that one
             // instruction covers whole row segments.  Rows that must not be
             // written (edges, masked tails, padding) are skipped.
-            if constexpr (!QOUT && kCols == 64) {
-                // 64-column warps: 32 rows x 128 bytes in the 128-byte
-                // swizzled order of the output's TMA store (chunk c of row r
-                // at c ^ (r & 7), so the lanes' 16-byte writes fall in
-                // distinct banks), 4 KiB per warp on a 1 KiB boundary.  When
-                // all 32 rows are stored, one TMA store writes them (clipped
-                // at the N edge) and the warp moves on; otherwise (edges,
-                // masked tails, padding) the warp stores the rows it owns.
-                const uint32_t st0 = smem_u32(smem + L::kOutOff) + (warp - kEpiWarp0) * 4096;
+            if constexpr (!QOUT) {
+                // Each warp stages its 32 rows x kCols bf16 (kRowB bytes a
+                // row) in the swizzled order of the output's TMA store, so
+                // that the lanes' 16-byte writes fall in distinct banks:
+                // 16-byte chunk c of row r sits at c ^ (r & 7) in 128-byte
+                // rows (64 columns, 128-byte swizzle) and at c ^ ((r >> 1) & 3)
+                // in 64-byte rows (32 columns, 64-byte swizzle).  When all 32
+                // rows are stored, one TMA store writes them (clipped at the N
+                // edge) and the warp moves on; otherwise (edges, masked tails,
+                // padding) the warp stores the rows it owns.
+                constexpr int kRowB = kCols * 2;
+                constexpr int kRowChunks = kRowB / 16;
+                auto swz = [](int rr) { return kRowB == 128 ? (rr & 7) : ((rr >> 1) & 3); };
+                const uint32_t st0 = smem_u32(smem + L::kOutOff) + (warp - kEpiWarp0) * (32 * kRowB);
                 if (lane == 0)
                     bulk_wait_group_read0();      // the previous tile's store has read these rows
                 __syncwarp();
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st_shared_v4(st0 + lane * 128 + 16 * (c ^ (lane & 7)), pack_bf16x2(acc[c * 4 + 0].x, acc[c * 4 + 0].y),
+                for (int c = 0; c < kRowChunks; ++c)
+                    st_shared_v4(st0 + lane * kRowB + 16 * (c ^ swz(lane)), pack_bf16x2(acc[c * 4 + 0].x, acc[c * 4 + 0].y),
                                  pack_bf16x2(acc[c * 4 + 1].x, acc[c * 4 + 1].y),
                                  pack_bf16x2(acc[c * 4 + 2].x, acc[c * 4 + 2].y),
                                  pack_bf16x2(acc[c * 4 + 3].x, acc[c * 4 + 3].y));
@@ -666,41 +673,17 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1) __maxnreg__(
                     }
                 } else {
                     __syncwarp();
+                    constexpr int kRowsPerPass = 32 / kRowChunks;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int rr = i * 4 + (lane >> 3);
-                        const int cc = lane & 7;
+                    for (int i = 0; i < kRowChunks; ++i) {
+                        const int rr = i * kRowsPerPass + lane / kRowChunks;
+                        const int cc = lane % kRowChunks;
                         if (((rows_ok >> rr) & 1u) && cc * 8 < cols_left) {
-                            const uint4 v = ld_shared_v4(st0 + rr * 128 + 16 * (cc ^ (rr & 7)));
+                            const uint4 v = ld_shared_v4(st0 + rr * kRowB + 16 * (cc ^ swz(rr)));
                             st_global_v4(d + (warp_row0 + rr) * p.N + ti.n0 + c0 + cc * 8, v.x, v.y, v.z, v.w);
                         }
                     }
                 }
-            } else if constexpr (!QOUT) {
-                uint8_t *const stage = smem + L::kOutOff + (warp - kEpiWarp0) * L::kOutWarpBytes;
-                const uint32_t my_row = smem_u32(stage) + lane * L::kOutRowStride;
-#pragma unroll
-                for (int c = 0; c < kCols / 8; ++c)
-                    st_shared_v4(my_row + c * 16, pack_bf16x2(acc[c * 4 + 0].x, acc[c * 4 + 0].y),
-                                 pack_bf16x2(acc[c * 4 + 1].x, acc[c * 4 + 1].y),
-                                 pack_bf16x2(acc[c * 4 + 2].x, acc[c * 4 + 2].y),
-                                 pack_bf16x2(acc[c * 4 + 3].x, acc[c * 4 + 3].y));
-                __syncwarp();
-                const uint32_t rows_ok = __ballot_sync(0xffffffffu, row_ok);
-                const size_t warp_row0 = d_row - lane;           // D row of this warp's first row
-                constexpr int kChunksPerRow = kCols / 8;         // 16-byte chunks per staged row
-#pragma unroll
-                for (int i = 0; i < kChunksPerRow; ++i) {
-                    const int idx = i * 32 + lane;
-                    const int rr = idx / kChunksPerRow;
-                    const int cc = idx % kChunksPerRow;
-                    const int col = ti.n0 + c0 + cc * 8;
-                    if (((rows_ok >> rr) & 1u) && col < p.N) {
-                        const uint4 v = ld_shared_v4(smem_u32(stage) + rr * L::kOutRowStride + cc * 16);
-                        st_global_v4(d + (warp_row0 + rr) * p.N + col, v.x, v.y, v.z, v.w);
-                    }
-                }
-                __syncwarp();
             } else {
                 // Re-quantised output.  Each thread rounds its 64 values to
                 // bf16, stages them in its row of the warp's shared-memory
@@ -957,17 +940,19 @@ dg_status_t launch(int layout, const uint8_t *a, const float *sfa, const uint8_t
         if (st != DG_OK)
             return st;
     }
-    // D (bf16 output): [rows][N], masked [G x max_m][N]; box: one 64-column
-    // epilogue warp's 32 rows, 128-byte swizzled like its staging rows.  The
-    // re-quantised output has no bf16 D and never reads this map.
+    // D (bf16 output): [rows][N], masked [G x max_m][N]; box: one epilogue
+    // warp's 32 rows x its columns (64 at 128-byte swizzle, 32 at 64-byte),
+    // swizzled like its staging rows.  The re-quantised output has no bf16 D
+    // and never reads this map.
     CUtensorMap td{};
     if (d) {
+        const int epi_cols = pl.bn == 192 ? kCfg192.epi_cols : pl.bn == 96 ? kCfg96.epi_cols : kCfg128.epi_cols;
         const uint64_t rows = layout == DG_LAYOUT_MASKED ? static_cast<uint64_t>(G) * M : static_cast<uint64_t>(M);
         const uint64_t dims[2] = {static_cast<uint64_t>(N), rows};
         const uint64_t strides[1] = {static_cast<uint64_t>(N) * 2};
-        const uint32_t box[2] = {64, 32};
+        const uint32_t box[2] = {static_cast<uint32_t>(epi_cols), 32};
         st = encode_tensor_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, dims, strides, box,
-                               CU_TENSOR_MAP_SWIZZLE_128B);
+                               epi_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
         if (st != DG_OK)
             return st;
     }
