@@ -9,10 +9,10 @@
 //     acc[m,n] = fmaf(P_kb[m,n], sfa[kb][m] * sfb[n/128][kb], acc[m,n]),
 // kb ascending; D = bf16_rn(acc).  The results are the same bits.
 //
-// Why a pair.  On GB300 one SM takes in at most ~73 bytes per cycle from L2
-// through TMA, and a TMA copy costs its SM a few hundred cycles whatever its
-// size, while the FP8 tensor core consumes a 128-row K block of A and of B
-// per 2N cycles.  A 128 x 192 tile (one SM) needs 104 bytes per cycle; in a
+// Why a pair.  On GB300 one SM takes in at most ~80 bytes per cycle from L2
+// through TMA (with two or three issuing threads; one thread reaches 63-70),
+// while the FP8 tensor core consumes a 128-row K block of A and of B per 2N
+// cycles.  A 128 x 192 tile (one SM) needs 104 bytes per cycle; in a
 // pair each SM holds its own 128 rows of A and half of B's 256 rows, so a
 // K block brings 32 KB per SM per 512 MMA cycles (63 bytes per cycle), moved
 // as 32 KB boxes (two K blocks per copy).
