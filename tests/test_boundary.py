@@ -74,6 +74,8 @@ def test_gemm_validation(lib):
     # masked: G limit and alignment of masked_m
     assert call(lib, "dg_fp8_grouped_masked", F, F, F, F, F, F, 5000, 256, 256, 512, 0, None) == \
         dg.DG_ERR_UNSUPPORTED_SHAPE
+    assert call(lib, "dg_fp8_grouped_masked", F, F, F, F, F, F, 1025, 256, 256, 512, 0, None) == \
+        dg.DG_ERR_UNSUPPORTED_SHAPE    # one expert past the device-side tile prefix
     assert call(lib, "dg_fp8_grouped_masked", F, F, F, F, F, F + 4, 4, 256, 256, 512, 0, None) == \
         dg.DG_ERR_MISALIGNED
     assert call(lib, "dg_fp8_grouped_masked", F, F, F, F, F, F, 4, 0, 256, 512, 0, None) == dg.DG_ERR_INVALID_ARG
