@@ -106,3 +106,57 @@ def test_masked_at_expert_capacity(expected_m):
     assert dg.dg_read_device_status() == 0
     ref = oracle.grouped_masked(a, sfa, b, sfb, masked_m, d=np.full((G, max_m, N), SENT, np.uint16))
     np.testing.assert_array_equal(out, ref)
+
+
+# Operands with more than 2^31 elements: every element and byte offset in the
+# kernels is 64-bit, which these tests check on the rows whose elements start
+# past 2^31 (a 32-bit offset would wrap there).  The operands are generated on
+# the device; the oracle gets only the sampled rows.
+def rows_around(r0: int, M: int, seed: int) -> np.ndarray:
+    return wl.sample_rows(M, 12, seed, must=[0, r0 - 1, r0, r0 + 1, M - 2, M - 1])
+
+
+def test_quantiser_past_2g_elements():
+    K = 8192
+    r0 = (1 << 31) // K                       # the first row whose elements start at 2^31
+    M = r0 + 64
+    gen = torch.Generator(device="cuda").manual_seed(31)
+    x = torch.randn((M, K), generator=gen, device="cuda", dtype=torch.float32)
+    q, sfa = dg.dg_quant_act_1x128(x)
+    torch.cuda.synchronize()
+    rows = rows_around(r0, M, 31)
+    idx = torch.from_numpy(rows).cuda()
+    x_rows = x.index_select(0, idx).cpu().numpy()
+    q_rows = q.index_select(0, idx).cpu().numpy()
+    s_rows = sfa[:, idx].cpu().numpy()
+    del x, q, sfa
+    torch.cuda.empty_cache()
+    ref_q, ref_s = oracle.quant_act_1x128(x_rows)
+    np.testing.assert_array_equal(q_rows, ref_q)
+    np.testing.assert_array_equal(s_rows, ref_s[:, :len(rows)])
+
+
+def test_dense_gemm_past_2g_operand():
+    N, K = 256, 7296
+    r0 = -(-(1 << 31) // K)                   # the first row whose elements start past 2^31
+    M = (r0 // 256 + 1) * 256                 # whole 256-row pair tiles
+    assert M * K > (1 << 31)
+    gen = torch.Generator(device="cuda").manual_seed(32)
+    # values +1 / -1 (E4M3 0x38 / 0xB8) and power-of-two scales: exact sums
+    a = torch.randint(0, 2, (M, K), generator=gen, device="cuda", dtype=torch.uint8).mul_(128).add_(0x38)
+    b = torch.randint(0, 2, (N, K), generator=gen, device="cuda", dtype=torch.uint8).mul_(128).add_(0x38)
+    g = np.random.default_rng(32)
+    sfa = wl.exact_scales(g, (K // QB, M))
+    sfb = wl.exact_scales(g, (-(-N // QB), K // QB))
+    d = dg.dg_fp8_gemm_nt(a, dev(sfa), b, dev(sfb))
+    out = bits(d)
+    assert dg.dg_read_device_status() == 0
+    rows = rows_around(r0, M, 32)
+    a_rows = a.index_select(0, torch.from_numpy(rows).cuda()).cpu().numpy()
+    b_h = b.cpu().numpy()
+    del a, d
+    torch.cuda.empty_cache()
+    sfa_rows = np.zeros((K // QB, oracle.round_up(len(rows), 4)), np.float32)
+    sfa_rows[:, :len(rows)] = sfa[:, rows]
+    ref = oracle.gemm_nt(a_rows, sfa_rows, b_h, sfb)
+    np.testing.assert_array_equal(out[rows], ref)
