@@ -162,7 +162,9 @@ dg_status_t dg_fp8_grouped_masked(const uint8_t *a, const float *sfa, const uint
  * bit for bit.  Rows not written by the bf16 call (padding, masked tails)
  * keep their q bytes and sfo entries.  N must be a multiple of 128
  * (DG_ERR_UNSUPPORTED_SHAPE); q and sfo 16-byte aligned (DG_ERR_MISALIGNED).
- * The tiles are 128 x 128 whatever the plan says for the bf16 call. */
+ * Dense and contiguous problems take the bf16 call's CTA-pair tiles where its
+ * plan has them (256 x 256; DG_FORCE_BN=128 or 256 pins the choice), every
+ * other problem 128 x 128 tiles on one SM. */
 dg_status_t dg_fp8_gemm_nt_q(const uint8_t *a, const float *sfa, const uint8_t *b, const float *sfb,
                              uint8_t *q, float *sfo, int M, int N, int K, void *stream);
 dg_status_t dg_fp8_grouped_contiguous_q(const uint8_t *a, const float *sfa, const uint8_t *b,

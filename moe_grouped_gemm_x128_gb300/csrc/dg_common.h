@@ -41,9 +41,9 @@ constexpr int kPairMaxRows = 1024;
 bool pair_plan_ok(int layout, int M, int N, int K, int G, int num_sms);
 int pair_smem_bytes();
 int pair_num_tiles(int layout, int M, int N, int G);
-dg_status_t launch_pair(int layout, const uint8_t *a, const float *sfa, const uint8_t *b, const float *sfb,
-                        uint16_t *d, const int32_t *meta, int M, int N, int K, int G, int num_tiles_hint, void *stream,
-                        const DeviceInfo &info);
+dg_status_t launch_pair(int layout, const uint8_t *a, const float *sfa, const uint8_t *b, const float *sfb, uint16_t *d,
+                        uint8_t *qout, float *sfo, const int32_t *meta, int M, int N, int K, int G,
+                        int num_tiles_hint, void *stream, const DeviceInfo &info);
 
 inline bool aligned16(const void *p)
 {

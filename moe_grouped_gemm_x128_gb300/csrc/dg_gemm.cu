@@ -831,13 +831,16 @@ int smem_for(int bn)
 Plan make_plan(int layout, int M, int N, int K, int G, int num_sms, bool qout = false, int expected_m = 0)
 {
     Plan pl;
-    // The CTA-pair kernel (256 x 256 tiles on two SMs) for bf16 output when
-    // the problem fills at least one wave of pairs and K is long enough
-    // (at least 16 K blocks) to amortise a tile's ring fill and store: it
-    // takes in 63 bytes per SM cycle at the FP8 tensor rate, which one SM's
-    // TMA can sustain, where the one-SM tiles need 94-128.
-    const int fb = qout ? 0 : forced_bn();
-    if (!qout && pair_plan_ok(layout, M, N, K, G, num_sms) &&
+    // The CTA-pair kernel (256 x 256 tiles on two SMs) when the problem fills
+    // at least one wave of pairs and K is long enough (at least 16 K blocks)
+    // to amortise a tile's ring fill and store: it takes in 63 bytes per SM
+    // cycle at the FP8 tensor rate, which one SM's TMA can sustain, where the
+    // one-SM tiles need 94-128.  Its 128-column scale groups lie inside a
+    // tile, so it also writes the re-quantised output.
+    int fb = forced_bn();
+    if (qout && fb != 256 && fb != 128)
+        fb = 0;
+    if (pair_plan_ok(layout, M, N, K, G, num_sms) &&
         (fb == 256 || (fb == 0 && K >= 16 * kBK && pair_num_tiles(layout, M, N, G) >= num_sms / 2))) {
         pl.bm = 256;
         pl.bn = 256;
@@ -908,7 +911,7 @@ dg_status_t launch(int layout, const uint8_t *a, const float *sfa, const uint8_t
     const bool qmode = qout != nullptr;
     const Plan pl = make_plan(layout, M, N, K, G, info.sm_count, qmode, expected_m);
     if (pl.bm == 256)
-        return launch_pair(layout, a, sfa, b, sfb, d, meta, M, N, K, G, pl.num_tiles, stream, info);
+        return launch_pair(layout, a, sfa, b, sfb, d, qout, sfo, meta, M, N, K, G, pl.num_tiles, stream, info);
     const int ldsfa = round_up(M, 4);
 
     // Tensor maps view each K-major operand as [..][rows][K/128][128 bytes]:

@@ -79,14 +79,18 @@ struct PairSmem {
     // stage's two K blocks and the two sfb values of its column block
     static constexpr int kScaleWarpBytes = 2 * (2 * 32 + 4) * 4;
     static constexpr int kScaleOff = kOutOff + kPEpiWarps * kOutWarpBytes;
-    static constexpr int kBarOff = kScaleOff + kPEpiWarps * kScaleWarpBytes;
-    // full[S], empty[S], tfull[2], tempty[2], drain[2]
-    static constexpr int kNumBars = 2 * kPStages + 6;
-    static constexpr int kMiscOff = kBarOff + 128;             // tmem base, abort flag, pair-row count
+    // re-quantised output: each row's amax over its 64 columns, per column
+    // slice and tile parity, exchanged between the two slices of a
+    // 128-column scale group
+    static constexpr int kAmaxOff = kScaleOff + kPEpiWarps * kScaleWarpBytes;
+    static constexpr int kBarOff = kAmaxOff + 2 * (kPBN / kPEpiCols) * kPRowsCta * 4;
+    // full[S], empty[S], tfull[2], tempty[2], drain[2], xchg[4 quarters x 2 groups]
+    static constexpr int kNumBars = 2 * kPStages + 6 + 8;
+    static constexpr int kMiscOff = kBarOff + 256;             // tmem base, abort flag, pair-row count
     static constexpr int kListOff = kMiscOff + 16;
     static constexpr int kBytes = kListOff + kPairMaxRows * 4;
     static constexpr int kAlloc = kBytes + 1024;              // slack to align the base to 1024
-    static_assert(kNumBars * 8 <= 128, "barrier area");
+    static_assert(kNumBars * 8 <= 256, "barrier area");
 };
 
 struct PairProblem {
@@ -135,10 +139,16 @@ __device__ __forceinline__ PairTile pair_tile(int t, int rows_p, int n_blocks, i
     return ti;
 }
 
+// QOUT: instead of bf16 D, write D re-quantised as the next GEMM's activation
+// operand (E4M3 codes in D's layout and one fp32 scale per 1x128 group of each
+// row, M-major), each group computed from the bf16-rounded values exactly as
+// the 1x128 quantiser does; the same output as fp8_gemm_kernel's.
+template <bool QOUT>
 __global__ void __launch_bounds__(kPThreads, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                          const __grid_constant__ CUtensorMap tmap_d,
                          const float *__restrict__ sfa, const float *__restrict__ sfb, uint16_t *__restrict__ d,
+                         uint8_t *__restrict__ qout, float *__restrict__ sfo,
                          const int32_t *__restrict__ meta, PairProblem p, unsigned int *status)
 {
     using L = PairSmem;
@@ -151,6 +161,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     auto tfull_bar = [&](int i) { return bar0 + 8u * (2 * kPStages + i); };
     auto tempty_bar = [&](int i) { return bar0 + 8u * (2 * kPStages + 2 + i); };
     auto drain_bar = [&](int i) { return bar0 + 8u * (2 * kPStages + 4 + i); };
+    // the two 64-column slices of 128-column scale group h in lane quarter q
+    auto xchg_bar = [&](int q, int h) { return bar0 + 8u * (2 * kPStages + 6 + 2 * q + h); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::kMiscOff + 4);
     int *num_rows_s = reinterpret_cast<int *>(smem + L::kMiscOff + 8);
@@ -181,6 +193,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mbar_init(tempty_bar(i), 2 * kPEpiWarps);
             mbar_init(drain_bar(i), 1);
         }
+        if constexpr (QOUT)
+            for (int i = 0; i < 8; ++i)
+                mbar_init(xchg_bar(i >> 1, i & 1), 64);
         *abort_flag = 0;
         fence_mbarrier_init();
         fence_proxy_async_smem();
@@ -337,6 +352,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const uint32_t stage_u32 = sbase + L::kOutOff + (warp - kPEpiWarp0) * L::kOutWarpBytes;
         const uint32_t scale_u32 = sbase + L::kScaleOff + (warp - kPEpiWarp0) * L::kScaleWarpBytes;
         uint32_t gs = 0;
+        uint32_t tile_par = 0;   // alternates per tile (the re-quantised output's amax exchange)
         bool ok = true;
         for (int t = pair_id; ok && t < num_tiles; t += num_pairs) {
             const PairTile ti = pair_tile(t, rows_p, n_blocks, pM, player, list, meta, rank);
@@ -435,45 +451,114 @@ __global__ void __launch_bounds__(kPThreads, 1)
             cp_async_wait<0>();
             if (!ok)
                 break;
-            // bf16 first: the 64 accumulators become 32 packed words
-            uint32_t pk[kPEpiCols / 2];
+            if constexpr (!QOUT) {
+                // bf16 first: the 64 accumulators become 32 packed words
+                uint32_t pk[kPEpiCols / 2];
 #pragma unroll
-            for (int k = 0; k < kPEpiCols / 2; ++k)
-                pk[k] = pack_bf16x2(acc[k].x, acc[k].y);
-            const uint32_t rows_ok = __ballot_sync(0xffffffffu, row_ok);
-            const int cols_left = pN - (ti.n0 + c0);
-            // The warp's 32 rows x 64 columns go into its staging rows in the
-            // 128-byte swizzled order (chunk c of row r at c ^ (r & 7): the
-            // lanes' 16-byte writes fall in distinct banks).  When all 32 rows
-            // are stored, one TMA store writes them (clipped at the M and N
-            // edges) and the warp moves on; otherwise (contiguous padding
-            // rows, a rank with no rows) the warp stores the rows it owns.
-            if (lane == 0)
-                bulk_wait_group_read0();        // the previous tile's store has read the staging rows
-            __syncwarp();
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                st_shared_v4(stage_u32 + lane * 128 + 16 * (c ^ (lane & 7)), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                             pk[4 * c + 3]);
-            if (rows_ok == 0xFFFFFFFFu && cols_left > 0) {
-                fence_proxy_async_smem();       // the writes above, visible to the TMA engine
+                for (int k = 0; k < kPEpiCols / 2; ++k)
+                    pk[k] = pack_bf16x2(acc[k].x, acc[k].y);
+                const uint32_t rows_ok = __ballot_sync(0xffffffffu, row_ok);
+                const int cols_left = pN - (ti.n0 + c0);
+                // The warp's 32 rows x 64 columns go into its staging rows in the
+                // 128-byte swizzled order (chunk c of row r at c ^ (r & 7): the
+                // lanes' 16-byte writes fall in distinct banks).  When all 32 rows
+                // are stored, one TMA store writes them (clipped at the M and N
+                // edges) and the warp moves on; otherwise (contiguous padding
+                // rows, a rank with no rows) the warp stores the rows it owns.
+                if (lane == 0)
+                    bulk_wait_group_read0();        // the previous tile's store has read the staging rows
                 __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&tmap_d, stage_u32, ti.n0 + c0, ti.m_cta + q * 32);
-                    bulk_commit_group();
-                }
-            } else {
-                __syncwarp();
-                uint16_t *const d_warp = d + static_cast<size_t>(ti.m_cta + q * 32) * pN + ti.n0 + c0;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int rr = i * 4 + (lane >> 3);
-                    const int cc = lane & 7;
-                    if (((rows_ok >> rr) & 1u) && cc * 8 < cols_left) {
-                        const uint4 v = ld_shared_v4(stage_u32 + rr * 128 + 16 * (cc ^ (rr & 7)));
-                        st_global_v4(d_warp + static_cast<size_t>(rr) * pN + cc * 8, v.x, v.y, v.z, v.w);
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(stage_u32 + lane * 128 + 16 * (c ^ (lane & 7)), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                                 pk[4 * c + 3]);
+                if (rows_ok == 0xFFFFFFFFu && cols_left > 0) {
+                    fence_proxy_async_smem();       // the writes above, visible to the TMA engine
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmap_d, stage_u32, ti.n0 + c0, ti.m_cta + q * 32);
+                        bulk_commit_group();
+                    }
+                } else {
+                    __syncwarp();
+                    uint16_t *const d_warp = d + static_cast<size_t>(ti.m_cta + q * 32) * pN + ti.n0 + c0;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = i * 4 + (lane >> 3);
+                        const int cc = lane & 7;
+                        if (((rows_ok >> rr) & 1u) && cc * 8 < cols_left) {
+                            const uint4 v = ld_shared_v4(stage_u32 + rr * 128 + 16 * (cc ^ (rr & 7)));
+                            st_global_v4(d_warp + static_cast<size_t>(rr) * pN + cc * 8, v.x, v.y, v.z, v.w);
+                        }
                     }
                 }
+            } else {
+                // Re-quantised output.  The row's 64 values, rounded to bf16,
+                // give this slice's amax; the two slices of a 128-column group
+                // (column slices 2h and 2h + 1 of the same lane quarter) meet
+                // at xchg_bar(q, h), one phase per tile, and take the larger.
+                // Then the scale s = max(amax, 1e-4) / 448 (IEEE division),
+                // the codes E4M3(v / s) by the corrected reciprocal, staged in
+                // 64-byte swizzled rows and stored row segment by row segment.
+                auto unpack = [](uint32_t w) {
+                    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+                };
+                uint32_t pk[kPEpiCols / 2];
+                float mx = 0.0f;
+#pragma unroll
+                for (int k = 0; k < kPEpiCols / 2; ++k) {
+                    pk[k] = pack_bf16x2(acc[k].x, acc[k].y);
+                    const float2 v = unpack(pk[k]);
+                    mx = fmaxf(mx, fmaxf(fabsf(v.x), fabsf(v.y)));
+                }
+                const int h = grp >> 1;
+                float *const amax_x = reinterpret_cast<float *>(smem + L::kAmaxOff) +
+                                      tile_par * (kPBN / kPEpiCols) * kPRowsCta;
+                amax_x[grp * kPRowsCta + r] = mx;
+                mbar_arrive(xchg_bar(q, h));
+                if (!__all_sync(0xffffffffu, wait_phase(xchg_bar(q, h), tile_par, abort_flag, status))) {
+                    ok = false;
+                    break;
+                }
+                const float amax = fmaxf(mx, amax_x[(grp ^ 1) * kPRowsCta + r]);
+                const float sc = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
+                const float rsc = __frcp_rn(sc);
+                const uint32_t rows_ok = __ballot_sync(0xffffffffu, row_ok);
+                const int cols_left = pN - (ti.n0 + c0);
+                // 32 rows x 64 codes: chunk c (16 bytes) of row rr at c ^ ((rr >> 1) & 3)
+                __syncwarp();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t wd[4];
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const float2 v0 = div2_rn(unpack(pk[8 * c + 4 * k + 0]), sc, rsc);
+                        const float2 v1 = div2_rn(unpack(pk[8 * c + 4 * k + 1]), sc, rsc);
+                        const float2 v2 = div2_rn(unpack(pk[8 * c + 4 * k + 2]), sc, rsc);
+                        const float2 v3 = div2_rn(unpack(pk[8 * c + 4 * k + 3]), sc, rsc);
+                        wd[2 * k] = e4m3x4(v0.x, v0.y, v1.x, v1.y);
+                        wd[2 * k + 1] = e4m3x4(v2.x, v2.y, v3.x, v3.y);
+                    }
+                    st_shared_v4(stage_u32 + lane * 64 + 16 * (c ^ ((lane >> 1) & 3)), wd[0], wd[1], wd[2], wd[3]);
+                }
+                __syncwarp();
+                if (cols_left > 0) {
+                    uint8_t *const q_warp = qout + static_cast<size_t>(ti.m_cta + q * 32) * pN + ti.n0 + c0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int rr = i * 8 + (lane >> 2);
+                        const int cc = lane & 3;
+                        if ((rows_ok >> rr) & 1u) {
+                            const uint4 v = ld_shared_v4(stage_u32 + rr * 64 + 16 * (cc ^ ((rr >> 1) & 3)));
+                            st_global_v4(q_warp + static_cast<size_t>(rr) * pN + cc * 16, v.x, v.y, v.z, v.w);
+                        }
+                    }
+                    // one scale per row and 128-column group, M-major like sfa
+                    if ((grp & 1) == 0 && row_ok)
+                        sfo[static_cast<size_t>((ti.n0 >> 7) + h) * pldsfa + m] = sc;
+                }
+                __syncwarp();
+                tile_par ^= 1u;
             }
         }
         // every bulk store of this thread has completed before the CTA ends
@@ -527,8 +612,8 @@ int pair_num_tiles(int layout, int M, int N, int G)
 }
 
 dg_status_t launch_pair(int layout, const uint8_t *a, const float *sfa, const uint8_t *b, const float *sfb, uint16_t *d,
-                        const int32_t *meta, int M, int N, int K, int G, int num_tiles_hint, void *stream,
-                        const DeviceInfo &info)
+                        uint8_t *qout, float *sfo, const int32_t *meta, int M, int N, int K, int G,
+                        int num_tiles_hint, void *stream, const DeviceInfo &info)
 {
     const uint64_t KB = static_cast<uint64_t>(K / 128);
     CUtensorMap ta, tb;
@@ -553,10 +638,11 @@ dg_status_t launch_pair(int layout, const uint8_t *a, const float *sfa, const ui
         if (st != DG_OK)
             return st;
     }
-    CUtensorMap td;
-    {
+    CUtensorMap td{};
+    if (d) {
         // D: bf16 [M][N]; box: 64 columns x 32 rows (one epilogue warp's part
-        // of a tile), 128-byte swizzled like the staging rows
+        // of a tile), 128-byte swizzled like the staging rows.  The
+        // re-quantised output has no bf16 D and never reads this map.
         const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
         const uint64_t strides[1] = {static_cast<uint64_t>(N) * 2};
         const uint32_t box[2] = {static_cast<uint32_t>(kPEpiCols), 32};
@@ -565,7 +651,9 @@ dg_status_t launch_pair(int layout, const uint8_t *a, const float *sfa, const ui
         if (st != DG_OK)
             return st;
     }
-    st = ensure_smem_attr(reinterpret_cast<const void *>(fp8_gemm_pair_kernel), PairSmem::kAlloc);
+    const bool qmode = qout != nullptr;
+    auto kernel = qmode ? fp8_gemm_pair_kernel<true> : fp8_gemm_pair_kernel<false>;
+    st = ensure_smem_attr(reinterpret_cast<const void *>(kernel), PairSmem::kAlloc);
     if (st != DG_OK)
         return st;
     const int max_pairs = info.sm_count / 2;
@@ -585,7 +673,7 @@ dg_status_t launch_pair(int layout, const uint8_t *a, const float *sfa, const ui
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, fp8_gemm_pair_kernel, ta, tb, td, sfa, sfb, d, meta, prob, info.status_word) !=
+    if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, td, sfa, sfb, d, qout, sfo, meta, prob, info.status_word) !=
         cudaSuccess)
         return DG_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;

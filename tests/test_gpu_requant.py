@@ -28,6 +28,16 @@ def built():
     dg.dg_read_device_status()
 
 
+@pytest.fixture(params=["128", "256"], ids=["bn128", "pair256"])
+def qtile(request, monkeypatch):
+    """Runs the test on the one-SM 128 x 128 tiles and on the CTA-pair 256 x
+    256 tiles (DG_FORCE_BN; the masked layout keeps the one-SM tiles).  The
+    two-call pipelines the random cases compare with use the same tiles, so
+    that both sides see the tensor core's same summation."""
+    monkeypatch.setenv("DG_FORCE_BN", request.param)
+    return request.param
+
+
 def dev(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
@@ -47,12 +57,10 @@ def q_sf_sentinels(q_shape, sf_shape):
     return np.full(q_shape, Q_SENTINEL, np.uint8), np.full(sf_shape, SF_SENTINEL, np.float32)
 
 
-def unfused_dense(a, sfa, b, sfb, monkeypatch):
-    """The GPU's two-call pipeline on 128-wide tiles: bf16 D, then the 1x128
-    quantiser of D."""
-    monkeypatch.setenv("DG_FORCE_BN", "128")
+def unfused_dense(a, sfa, b, sfb):
+    """The GPU's two-call pipeline on the tiles DG_FORCE_BN names: bf16 D,
+    then the 1x128 quantiser of D."""
     d = dg.dg_fp8_gemm_nt(dev(a), dev(sfa), dev(b), dev(sfb))
-    monkeypatch.delenv("DG_FORCE_BN")
     q, sfo = dg.dg_quant_act_1x128(d)
     return host(d.view(torch.int16)).view(np.uint16), host(q), host(sfo)
 
@@ -97,7 +105,7 @@ DENSE_Q_SHAPES = [(128, 256, 512), (1, 128, 128), (129, 384, 384), (300, 640, 64
 
 
 @pytest.mark.parametrize("M,N,K", DENSE_Q_SHAPES)
-def test_dense_q_exact_bit_identical(M, N, K):
+def test_dense_q_exact_bit_identical(M, N, K, qtile):
     a, sfa, b, sfb = exact_dense(M, N, K, seed=M * 7 + N + K)
     q, sfo = q_sf_buffers((M, N), (N // QB, oracle.round_up(M, 4)))
     dg.dg_fp8_gemm_nt_q(dev(a), dev(sfa), dev(b), dev(sfb), q, sfo)
@@ -108,10 +116,10 @@ def test_dense_q_exact_bit_identical(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(300, 640, 1024), (129, 256, 2048), (1024, 1536, 512)])
-def test_dense_q_random_equals_two_call_pipeline(M, N, K, monkeypatch):
+def test_dense_q_random_equals_two_call_pipeline(M, N, K, qtile):
     a, sfa, b, sfb = random_dense(M, N, K, seed=M + 3 * N + K, outliers=True)
     q, sfo = dg.dg_fp8_gemm_nt_q(dev(a), dev(sfa), dev(b), dev(sfb))
-    d2, q2, sfo2 = unfused_dense(a, sfa, b, sfb, monkeypatch)
+    d2, q2, sfo2 = unfused_dense(a, sfa, b, sfb)
     np.testing.assert_array_equal(host(q), q2)
     np.testing.assert_array_equal(host(sfo), sfo2)
     q_ref, sfo_ref = oracle.gemm_nt_quant(a, sfa, b, sfb)
@@ -155,7 +163,7 @@ def contiguous_case(G, tokens, N, K, seed):
 
 
 @pytest.mark.parametrize("G,tokens,N,K", [(4, 700, 256, 512), (3, 129, 128, 128), (8, 1500, 384, 384)])
-def test_contiguous_q_exact_bit_identical(G, tokens, N, K):
+def test_contiguous_q_exact_bit_identical(G, tokens, N, K, qtile):
     a, sfa, b, sfb, mi = contiguous_case(G, tokens, N, K, seed=G * 5 + tokens)
     sum_M = a.shape[0]
     q, sfo = q_sf_buffers((sum_M, N), (N // QB, sum_M))
@@ -169,14 +177,13 @@ def test_contiguous_q_exact_bit_identical(G, tokens, N, K):
     assert pad.any() and np.all(q[pad] == Q_SENTINEL) and np.all(sfo[:, pad] == SF_SENTINEL)
 
 
-def test_contiguous_q_random_equals_two_call_pipeline(monkeypatch):
+def test_contiguous_q_random_equals_two_call_pipeline(qtile):
     G, tokens, N, K = 6, 900, 512, 1024
     counts, mi, seg = wl.contiguous_routing(G, tokens, seed=77)
     g = np.random.default_rng(78)
     a, sfa = oracle.quant_act_1x128(wl.normal_matrix(g, (len(mi), K), outliers=True))
     b, sfb = oracle.quant_weight_128x128(wl.normal_matrix(g, (G, N, K)))
     q, sfo = dg.dg_fp8_grouped_contiguous_q(dev(a), dev(sfa), dev(b), dev(sfb), dev(mi))
-    monkeypatch.setenv("DG_FORCE_BN", "128")
     d = dg.dg_fp8_grouped_contiguous(dev(a), dev(sfa), dev(b), dev(sfb), dev(mi))
     q2, sfo2 = dg.dg_quant_act_1x128(d)
     valid = mi >= 0
