@@ -405,9 +405,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     // fp32 product of the two scales, rounded once
                     const float sc = ld_shared_f32(buf + (i * 32 + lane) * 4) * ld_shared_f32(buf + (64 + i) * 4);
                     const float2 s2 = make_float2(sc, sc);
-                    // every lane polls (the warp sees one result per test;
-                    // cheaper than one poller and a broadcast)
-                    if (!__all_sync(0xffffffffu, wait_phase(tfull_bar(i), gs & 1u, abort_flag, status))) {
+                    // every lane polls and the warp votes on each test, so
+                    // that it leaves the wait converged for the warp-wide TMEM
+                    // loads (cheaper than one poller and a broadcast, and than
+                    // lanes that leave one by one)
+                    if (!wait_phase_warp(tfull_bar(i), gs & 1u, abort_flag, status)) {
                         ok = false;
                         break;
                     }
@@ -516,7 +518,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                                       tile_par * (kPBN / kPEpiCols) * kPRowsCta;
                 amax_x[grp * kPRowsCta + r] = mx;
                 mbar_arrive(xchg_bar(q, h));
-                if (!__all_sync(0xffffffffu, wait_phase(xchg_bar(q, h), tile_par, abort_flag, status))) {
+                if (!wait_phase_warp(xchg_bar(q, h), tile_par, abort_flag, status)) {
                     ok = false;
                     break;
                 }

@@ -51,6 +51,34 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
     return wait_phase_slow(bar, parity, abort_flag, status, limit);
 }
 
+// Bounded wait for the phase of `bar`, by a whole warp that stays converged:
+// every lane tests, and the warp leaves together once every lane has seen the
+// phase complete (the lanes then reach warp-wide instructions such as
+// tcgen05.ld without reconverging).  Same limit and abort rule as
+// wait_phase; returns the same value in every lane.
+__device__ __forceinline__ bool wait_phase_warp(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                                unsigned int *status, long long limit = kWaitTimeoutCycles)
+{
+    if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity)))
+        return true;
+    const long long t0 = clock64();
+    for (uint32_t it = 1;; ++it) {
+        if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity)))
+            return true;
+        if ((it & 63u) == 0) {
+            const bool aborted = *abort_flag != 0;
+            const bool late = clock64() - t0 > limit;
+            if (__any_sync(0xffffffffu, aborted || late)) {
+                if (__any_sync(0xffffffffu, late && !aborted) && (threadIdx.x & 31) == 0) {
+                    *abort_flag = 1;
+                    raise_status(status, DG_DEVFLAG_TIMEOUT);
+                }
+                return false;
+            }
+        }
+    }
+}
+
 // Bounded wait used while shutting down after an abort (ignores the flag).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long limit = kWaitTimeoutCycles)
 {
