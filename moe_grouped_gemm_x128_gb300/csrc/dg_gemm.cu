@@ -573,12 +573,12 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1) __maxnreg__(
                     const bool last_of_slot = (jj == KPS - 1) || (kb == KB - 1);
                     if (jj == 0) {
                         // wait until the MMAs of this stage are complete: every
-                        // lane polls and the warp votes on each test, so that it
-                        // leaves converged for the warp-wide TMEM loads (cheaper
-                        // than one poller and a broadcast).  No bar.sync /
+                        // lane polls (one test serves the warp; cheaper than one
+                        // poller and a broadcast; a vote on every test measured
+                        // slower here, unlike in the pair kernel).  No bar.sync /
                         // bar.warp.sync here: those order memory, which would
                         // make the scale loads issued ahead complete first.
-                        if (!wait_phase_warp(tfull_bar(buf), tph, abort_flag, status)) {
+                        if (!__all_sync(0xffffffffu, wait_phase(tfull_bar(buf), tph, abort_flag, status))) {
                             ok = false;
                             break;
                         }
