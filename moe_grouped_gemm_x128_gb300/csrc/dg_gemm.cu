@@ -24,13 +24,14 @@
 //               builds the masked layout's per-expert tile prefix;
 //   warps 4..   epilogue warpgroups, each owning EPI_COLS of the tile's
 //               columns; a thread owns one output row (TMEM lane).  Per slot
-//               lane 0 of each warp waits for the slot, the warp loads its
+//               every lane polls the slot's barrier, the warp loads its
 //               partial rows from TMEM and releases the slot, then scales each
 //               K block's row by sfa * sfb (read from global memory a few K
 //               blocks ahead into fixed registers) and FMAs it into fp32
-//               registers (two lanes per instruction), K blocks ascending;
-//               after the last block it converts to bf16, stages the rows in
-//               shared memory and stores them row-major.
+//               registers (two values per packed f32x2 instruction), K blocks
+//               ascending; after the last block it converts to bf16, stages
+//               the rows in shared memory and writes them with one TMA store
+//               per warp (row by row where some rows must not be written).
 // An mbarrier handoff costs a few hundred cycles, so handoffs are per stage
 // and per TMEM slot, not per MMA.  Tiles are 128 x 192 (4 one-K-block stages,
 // two TMEM slots, 512 threads) when the problem has at least a full wave of
