@@ -322,13 +322,6 @@ __device__ __forceinline__ void tmem_wait_ld32(uint32_t (&r)[32])
                  : "memory");
 }
 
-// One 32-bit column for the warp's 32 lanes: thread i writes lane
-// (base_lane + i) at column `taddr`.  Asynchronous until tmem_wait_st.
-__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v)
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
-}
-
 // Four consecutive 32-bit columns for the warp's 32 lanes (thread i writes
 // lane base_lane + i, columns taddr .. taddr + 3).
 __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3)
