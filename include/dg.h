@@ -164,7 +164,9 @@ dg_status_t dg_fp8_grouped_masked(const uint8_t *a, const float *sfa, const uint
  * (DG_ERR_UNSUPPORTED_SHAPE); q and sfo 16-byte aligned (DG_ERR_MISALIGNED).
  * Dense and contiguous problems take the bf16 call's CTA-pair tiles where its
  * plan has them (256 x 256; DG_FORCE_BN=128 or 256 pins the choice), every
- * other problem 128 x 128 tiles on one SM. */
+ * other problem 128 x 128 tiles on one SM.  The masked call's expected_m is
+ * accepted so that its arguments match dg_fp8_grouped_masked; its tiles are
+ * always 128 x 128, so the hint does not change its plan. */
 dg_status_t dg_fp8_gemm_nt_q(const uint8_t *a, const float *sfa, const uint8_t *b, const float *sfb,
                              uint8_t *q, float *sfo, int M, int N, int K, void *stream);
 dg_status_t dg_fp8_grouped_contiguous_q(const uint8_t *a, const float *sfa, const uint8_t *b,

@@ -1095,6 +1095,8 @@ extern "C" dg_status_t dg_fp8_grouped_masked_q(const uint8_t *a, const float *sf
         return DG_ERR_UNSUPPORTED_SHAPE;
     if (!dg::aligned16(masked_m))
         return DG_ERR_MISALIGNED;
+    // expected_m only sizes the bf16 call's tiles; a re-quantised output
+    // always takes 128 x 128 tiles, whatever the rows per expert
     return dg::launch(DG_LAYOUT_MASKED, a, sfa, b, sfb, nullptr, q, sfo, masked_m, max_m, N, K, G, stream);
 }
 
